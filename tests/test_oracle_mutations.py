@@ -1,0 +1,45 @@
+"""The oracle's pins catch plausible mistakes.
+
+Each case plants one mistake in a copy of oracle.c (on the CPU), builds it
+and runs the pin suite against it in a subprocess: the suite must fail.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "oracle.c")
+
+MUTATIONS = {
+    "skip_sign_flipped": ("(c < ln_lambda)", "(c > ln_lambda)"),
+    "vote_min_not_max": ("if (diff > c) c = diff;", "if (c == -INFINITY || diff < c) c = diff;"),
+    "l_not_rescaled": ("st->l[r] *= alpha;", ""),
+    "alpha_sign": ("exp(st->m[r] - m_new)", "exp(m_new - st->m[r])"),
+    "gqa_head_map": ("kvh = h / G;", "kvh = h % p->Hkv;"),
+    "causal_top_left": ("row + off : (int64_t)p->Lk - 1", "row : (int64_t)p->Lk - 1"),
+    "scale_dropped": ("x = scale * dot_bf16", "x = dot_bf16"),
+    "merge_weight_sign": ("exp(sm[(size_t)g * S + sp] - mstar)", "exp(mstar - sm[(size_t)g * S + sp])"),
+    "split_floor": ("T = ceil_div(nT, S)", "T = (nT / S > 0 ? nT / S : 1)"),
+    "calib_edge": ("a = L * exp(0.5 * (lo + hi));", "a = L * exp(lo);"),
+    "v_transposed": ("p * bf16_to_double(vk[e])", "p * bf16_to_double(vh[(size_t)e * d + (k0 + t) % d])"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_reject_mutation(name, tmp_path):
+    old, new = MUTATIONS[name]
+    src = open(SRC).read()
+    assert src.count(old) >= 1, f"mutation anchor not found: {old!r}"
+    mutated = tmp_path / "oracle.c"
+    mutated.write_text(src.replace(old, new))
+    (tmp_path / "oracle.h").write_text(open(os.path.join(ROOT, "oracle", "oracle.h")).read())
+    lib = tmp_path / "liboracle_mut.so"
+    subprocess.check_call(["gcc", "-O1", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", str(lib),
+                           str(mutated), "-lm"])
+    env = dict(os.environ, SSATTN_ORACLE_LIB=str(lib))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"mutation {name} survived the pins:\n{r.stdout[-2000:]}"
