@@ -1,1 +1,133 @@
-"""Skip-softmax (BLASST) attention for GB300 (sm_103a)."""
+"""Skip-softmax (BLASST) attention for GB300 (sm_103a).
+
+The product is the C-ABI library ``libssattn.so`` (``include/ssattn.h``);
+:mod:`.capi` binds its entry points under the same names.  The helpers below
+only allocate outputs with torch and forward to those entry points: every
+step of the attention pass runs in the library's CUDA kernels, and there is
+no CPU or eager fallback (a missing library raises).
+"""
+from __future__ import annotations
+
+import math
+
+from . import capi
+from .capi import SSError
+
+TILE = 128
+
+
+def build(force: bool = False) -> str:
+    from .builder import build as _build
+
+    return _build(force=force)
+
+
+def _check(st: int, what: str):
+    if st != capi.SS_OK:
+        raise SSError(st, what)
+
+
+def _shape_prefill(q, k):
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("prefill expects q [B,Hq,Lq,d] and k/v [B,Hkv,Lk,d]")
+    B, Hq, Lq, d = q.shape
+    Bk, Hkv, Lk, dk = k.shape
+    if Bk != B or dk != d:
+        raise ValueError("q and k disagree on batch or head dim")
+    return B, Hq, Hkv, Lq, Lk, d
+
+
+def units_prefill(B, Hq, Lq) -> int:
+    return B * Hq * math.ceil(Lq / TILE)
+
+
+def prefill(q, k, v, *, scale: float, causal: bool = False, lam: float = 0.0, counts=None,
+            out=None, skip_mask=None, vote_margin=None, stream=None):
+    """o = skip-softmax attention(q, k, v) for bf16 CUDA tensors.
+
+    q [B,Hq,Lq,d], k/v [B,Hkv,Lk,d] contiguous.  Returns o [B,Hq,Lq,d].
+    ``counts`` (uint32/int32 tensor of B*Hq*ceil(Lq/128)) receives the
+    skipped tiles per query block; ``skip_mask``/``vote_margin`` the
+    per-tile debug outputs."""
+    import torch
+
+    B, Hq, Hkv, Lq, Lk, d = _shape_prefill(q, k)
+    o = out if out is not None else torch.empty_like(q)
+    if skip_mask is None and vote_margin is None:
+        st = capi.ss_attn_prefill(q, k, v, o, B, Hq, Hkv, Lq, Lk, d, scale, causal, lam, counts,
+                                  stream)
+    else:
+        st = capi.ss_attn_prefill_ex(q, k, v, o, B, Hq, Hkv, Lq, Lk, d, scale, causal, lam,
+                                     counts, skip_mask, vote_margin, False, stream)
+    _check(st, "ss_attn_prefill")
+    return o
+
+
+def decode_workspace(B, Hq, d, num_kv_splits, device):
+    import torch
+
+    n = capi.ss_attn_decode_workspace_size(B, Hq, d, num_kv_splits)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device), n
+
+
+def decode(q, k, v, *, scale: float, lam: float = 0.0, num_kv_splits: int = 1, counts=None,
+           out=None, workspace=None, skip_mask=None, vote_margin=None, stream=None):
+    """Split-KV decode: q [B,Hq,d], k/v [B,Hkv,Lk,d] bf16 CUDA.  Returns o [B,Hq,d]."""
+    import torch
+
+    B, Hq, d = q.shape
+    _, Hkv, Lk, _ = k.shape
+    o = out if out is not None else torch.empty_like(q)
+    if workspace is None:
+        workspace, nbytes = decode_workspace(B, Hq, d, num_kv_splits, q.device)
+    else:
+        nbytes = workspace.numel() * workspace.element_size()
+    if skip_mask is None and vote_margin is None:
+        st = capi.ss_attn_decode(q, k, v, o, B, Hq, Hkv, Lk, d, scale, lam, num_kv_splits, counts,
+                                 workspace, nbytes, stream)
+    else:
+        st = capi.ss_attn_decode_ex(q, k, v, o, B, Hq, Hkv, Lk, d, scale, lam, num_kv_splits,
+                                    counts, workspace, nbytes, skip_mask, vote_margin, False,
+                                    stream)
+    _check(st, "ss_attn_decode")
+    return o
+
+
+def calibrate(kind: str, q, k, v, *, scale: float, target_sparsity: float, causal: bool = False,
+              num_kv_splits: int = 1, counts=None, stream=None):
+    """Fit a (lambda = a / Lk) for a target tile sparsity.  Returns (a, achieved)."""
+    import torch
+
+    if kind == "prefill":
+        B, Hq, Hkv, Lq, Lk, d = _shape_prefill(q, k)
+        n = units_prefill(B, Hq, Lq)
+        k_ = capi.SS_PREFILL
+    else:
+        B, Hq, d = q.shape
+        _, Hkv, Lk, _ = k.shape
+        Lq = 1
+        n = B * Hkv * num_kv_splits
+        k_ = capi.SS_DECODE
+    if counts is None:
+        counts = torch.empty(n, dtype=torch.int32, device=q.device)
+    prob = capi.ss_problem(k_, q.data_ptr(), k.data_ptr(), v.data_ptr(), B, Hq, Hkv, Lq, Lk, d,
+                           float(scale), int(bool(causal)), int(num_kv_splits), counts.data_ptr(),
+                           capi._stream(stream))
+    st, a, achieved = capi.ss_calibrate(prob, target_sparsity)
+    _check(st, "ss_calibrate")
+    return a, achieved
+
+
+def fit_factor(s, a):
+    st, A, B = capi.ss_fit_factor(s, a)
+    _check(st, "ss_fit_factor")
+    return A, B
+
+
+def lambda_of(A, B, s, L) -> float:
+    return capi.ss_lambda(A, B, s, L)
+
+
+def stream_status(stream=None) -> None:
+    st = capi.ss_stream_status(stream)
+    _check(st, "device status")

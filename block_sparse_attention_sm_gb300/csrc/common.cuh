@@ -1,0 +1,77 @@
+// Internal declarations shared by the kernels and the C-ABI layer.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cuda_bf16.h>
+
+#include "ssattn.h"
+
+namespace ssattn {
+
+constexpr int kTile = 128;  // key tile and prefill query block
+
+// Device status word: kernels that give up a bounded wait OR a code into the
+// word whose address the launch passes them (module memory of the C-ABI
+// layer, not an allocation); ss_stream_status reads and clears it.
+constexpr uint32_t kDevStatusTimeout = 1u;
+
+__device__ __forceinline__ void report_timeout(uint32_t* status) {
+  if (status != nullptr) atomicOr(status, kDevStatusTimeout);
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+enum class Mode : int { kDense = 0, kSparse = 1, kCount = 2 };
+
+struct PrefillParams {
+  int B, Hq, Hkv, Lq, Lk;
+  int G;          // Hq / Hkv
+  int nQB, nT;    // query blocks, key tiles
+  int causal;
+  float scale_log2;  // scale * log2(e): exponent factor on raw scores
+  float scale;       // natural-log factor (for margins)
+  float thr_raw;     // ln(lambda) / scale: skip iff tile_max - m < thr_raw (raw units)
+  __nv_bfloat16* o;
+  uint32_t* counts;
+  uint8_t* mask;
+  float* margin;
+  uint32_t* status;
+};
+
+struct DecodeParams {
+  int B, Hq, Hkv, Lk, d;
+  int G;
+  int nT, S, T;      // tiles, splits, tiles per split
+  float scale_log2;
+  float scale;
+  float thr_raw;
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
+  __nv_bfloat16* o;       // final output when S == 1
+  float* part;            // [B*Hq][S][d + 2] partial (O..., m, l) when S > 1
+  uint32_t* counts;
+  uint8_t* mask;
+  float* margin;
+  uint32_t* status;
+  int count_only;
+};
+
+// Launchers (return a CUDA error code; arguments are already validated).
+cudaError_t launch_prefill(int d, Mode mode, const CUtensorMap& tq, const CUtensorMap& tk,
+                           const CUtensorMap& tv, const PrefillParams& p, cudaStream_t st);
+cudaError_t launch_decode(const DecodeParams& p, Mode mode, cudaStream_t st);
+
+}  // namespace ssattn

@@ -1,0 +1,475 @@
+// Skip-softmax (BLASST) split-KV decode forward for sm_103a, plus the
+// log-sum-exp merge of the splits.
+//
+// Method (BLASST summary, §Methodologie and §Kernel-ontwerp; "Skip-Softmax"
+// design doc, §The skip test): decode is bound by HBM traffic.  Every K tile
+// of a split is streamed (the scores decide the skip), but a skipped tile's
+// V block is never loaded.  To keep the pipeline free of bubbles the
+// decisions are taken a chunk of tiles at a time and the surviving V tiles of
+// that chunk are fetched as one batch, while the next chunk's scores run.
+//
+// One CTA = one (sequence b, KV head, split); 256 threads (8 warps).  The G
+// query heads sharing the KV head (one token each) form the voting group:
+// a tile is skipped only if every one of them passes the test.
+//
+// Pipeline per chunk c of 2 tiles (iteration c):
+//   A(c)   scores of tiles 2c, 2c+1 (warps 0-3 / 4-7, 32 keys per warp) from
+//          the K ring (4 stages, 1-D bulk copies of contiguous 128-key tiles);
+//          then the two freed K stages are refilled 2 chunks ahead.
+//   C(c-1) online softmax + P.V over the survivors of chunk c-1 (their V
+//          tiles were issued at the end of the previous iteration).
+//   B(c)   per-row tile maxima, the vote (exact running maximum, one thread),
+//          counters / mask / margin, and the batch of V loads for chunk c's
+//          survivors.
+// Scores use fp32 FMAs on bf16 K read from shared memory (the contraction
+// has only G <= 8 rows; the kernel is bound by the K stream, not by math).
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "ptx_sm103.cuh"
+
+namespace ssattn {
+
+namespace {
+
+constexpr int kDecThreads = 256;
+constexpr int kKStages = 4;
+
+template <int D, int GP>
+struct DecodeCfg {
+  static constexpr int kTileBytes = kTile * D * 2;
+  static constexpr int kLPR = D / 8;           // lanes per key row (16-byte slices)
+  static constexpr int kKPI = 32 / kLPR;       // keys per warp iteration
+  static constexpr int kIters = 32 / kKPI;     // iterations for the warp's 32 keys
+  static constexpr int kNDP = D / 2;           // threads per key group in P.V (bf16 pairs)
+  static constexpr int kNKG = kDecThreads / kNDP;  // key groups
+  static constexpr int kKPG = kTile / kNKG;    // keys per group
+  // shared memory layout (bytes, 16-byte aligned pieces)
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kKOff + kKStages * kTileBytes;
+  static constexpr int kQOff = kVOff + 2 * kTileBytes;                 // float [GP][D]
+  static constexpr int kScOff = kQOff + GP * D * 4;                    // float [2][2][GP][128]
+  static constexpr int kPOff = kScOff + 2 * 2 * GP * kTile * 4;        // float [2][128][GP]
+  static constexpr int kTmOff = kPOff + 2 * kTile * GP * 4;            // float [2][2][GP]
+  static constexpr int kAlOff = kTmOff + 2 * 2 * GP * 4;               // float [2][GP]
+  static constexpr int kMlOff = kAlOff + 2 * GP * 4;                   // float [GP][2]
+  static constexpr int kCtlOff = (kMlOff + GP * 2 * 4 + 15) / 16 * 16;
+  static constexpr int kSmemBytes = kCtlOff + 128;
+  static_assert(kNKG * GP * D * 4 <= kKStages * kTileBytes, "reduction buffer must fit the K ring");
+};
+
+struct DecodeCtl {
+  uint64_t k_full[kKStages];
+  uint64_t v_full[2];
+  int abort_flag;
+  int n_surv;
+  int surv_tile[2];
+  uint32_t surv_par[2];
+};
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& raw, float (&f)[8]) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+template <int D, int GP, Mode MODE>
+__global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecodeParams p) {
+  using C = DecodeCfg<D, GP>;
+  constexpr bool kPV = (MODE != Mode::kCount);
+  constexpr bool kVote = (MODE != Mode::kDense);
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* sK = smem + C::kKOff;
+  uint8_t* sV = smem + C::kVOff;
+  float* sQ = reinterpret_cast<float*>(smem + C::kQOff);
+  float* sSc = reinterpret_cast<float*>(smem + C::kScOff);
+  float* sP = reinterpret_cast<float*>(smem + C::kPOff);
+  float* sTm = reinterpret_cast<float*>(smem + C::kTmOff);
+  float* sAl = reinterpret_cast<float*>(smem + C::kAlOff);
+  float* sMl = reinterpret_cast<float*>(smem + C::kMlOff);
+  auto* ctl = reinterpret_cast<DecodeCtl*>(smem + C::kCtlOff);
+  volatile int* abort_flag = &ctl->abort_flag;
+  auto SC = [&](int buf, int tl, int g) { return sSc + ((buf * 2 + tl) * GP + g) * kTile; };
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = p.G;
+  const int split = blockIdx.x % p.S;
+  const int bk = blockIdx.x / p.S;  // b * Hkv + kvh
+  const int b = bk / p.Hkv, kvh = bk - (bk / p.Hkv) * p.Hkv;
+  const int j0 = split * p.T;
+  const int nt = max(0, min(p.nT, j0 + p.T) - j0);
+  const int nchunks = (nt + 1) / 2;
+  const __nv_bfloat16* kbase = p.k + (static_cast<size_t>(bk) * p.Lk) * D;
+  const __nv_bfloat16* vbase = p.v + (static_cast<size_t>(bk) * p.Lk) * D;
+  auto tile_rows = [&](int t) { return min(kTile, p.Lk - (j0 + t) * kTile); };
+
+  if (tid == 0) {
+    for (int s = 0; s < kKStages; ++s) mbar_init(&ctl->k_full[s], 1);
+    for (int s = 0; s < 2; ++s) mbar_init(&ctl->v_full[s], 1);
+    ctl->abort_flag = 0;
+    ctl->n_surv = 0;
+    fence_mbar_init();
+  }
+  // Query rows of the group (fp32 copy; padding rows are zero).
+  for (int idx = tid; idx < GP * D; idx += kDecThreads) {
+    const int g = idx / D, e = idx - (idx / D) * D;
+    sQ[idx] = (g < G) ? __bfloat162float(p.q[(static_cast<size_t>(b) * p.Hq + kvh * G + g) * D + e]) : 0.f;
+  }
+  __syncthreads();
+
+  // Thread 0 owns every bulk copy.
+  int nk_issued = 0;
+  uint32_t nv_issued[2] = {0u, 0u};
+  auto issue_k = [&](int t) {
+    const int st = t % kKStages;
+    const uint32_t bytes = static_cast<uint32_t>(tile_rows(t)) * D * 2;
+    mbar_arrive_expect_tx(&ctl->k_full[st], bytes);
+    bulk_load(sK + st * C::kTileBytes, kbase + static_cast<size_t>(j0 + t) * kTile * D, bytes,
+              &ctl->k_full[st]);
+    nk_issued = t + 1;
+  };
+  if (tid == 0)
+    for (int t = 0; t < min(nt, kKStages); ++t) issue_k(t);
+
+  // Per-lane query slice for the score phase.
+  float qv[GP][8];
+  {
+    const int e0 = (lane % C::kLPR) * 8;
+#pragma unroll
+    for (int g = 0; g < GP; ++g)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) qv[g][e] = sQ[g * D + e0 + e];
+  }
+
+  // Running state.  Thread 0: exact running max per row for the vote.
+  // Warp g (< GP): softmax state of row g (all lanes hold the same values).
+  float mt[GP];
+#pragma unroll
+  for (int g = 0; g < GP; ++g) mt[g] = -INFINITY;
+  float m_run = -INFINITY, l_run = 0.f;
+  float acc[GP][2];
+#pragma unroll
+  for (int g = 0; g < GP; ++g) acc[g][0] = acc[g][1] = 0.f;
+  uint32_t skipped = 0;
+  const float sl2 = p.scale_log2;
+
+  for (int c = 0; c <= nchunks; ++c) {
+    const int cb = c & 1;
+    // ---------------------------------------------------------------- A(c)
+    if (c < nchunks) {
+      const int tl = warp >> 2;
+      const int t = 2 * c + tl;
+      if (t < nt) {
+        const int st = t % kKStages;
+        if (mbar_wait(&ctl->k_full[st], (t / kKStages) & 1, abort_flag)) {
+          const uint8_t* kt = sK + st * C::kTileBytes;
+          const int valid = tile_rows(t);
+          float* sc = SC(cb, tl, 0);
+#pragma unroll 4
+          for (int it = 0; it < C::kIters; ++it) {
+            const int key = (warp & 3) * 32 + it * C::kKPI + lane / C::kLPR;
+            const uint4 raw =
+                *reinterpret_cast<const uint4*>(kt + key * D * 2 + (lane % C::kLPR) * 16);
+            float kf[8];
+            bf16x8_to_f32(raw, kf);
+            float part[GP];
+#pragma unroll
+            for (int g = 0; g < GP; ++g) {
+              float a = 0.f;
+#pragma unroll
+              for (int e = 0; e < 8; ++e) a = fmaf(qv[g][e], kf[e], a);
+              part[g] = a;
+            }
+            // Transpose-reduce over the kLPR lanes of this key: each halving
+            // step hands half of the rows to the partner lane, so the lane
+            // ends up holding the full dot product of row `gsel`.
+            int gsel = 0;
+            bool writer = true;
+            int n = GP;
+#pragma unroll
+            for (int o = C::kLPR / 2; o >= 1; o >>= 1) {
+              const bool upper = (lane & o) != 0;
+              if (n > 1) {
+                const int hn = n / 2;
+#pragma unroll
+                for (int j = 0; j < GP / 2; ++j) {
+                  if (j < hn) {
+                    const float send = upper ? part[j] : part[j + hn];
+                    const float keep = upper ? part[j + hn] : part[j];
+                    part[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                  }
+                }
+                gsel += upper ? hn : 0;
+                n = hn;
+              } else {
+                part[0] += __shfl_xor_sync(0xffffffffu, part[0], o);
+                writer = writer && !upper;
+              }
+            }
+            if (writer && gsel < G) sc[gsel * kTile + key] = (key < valid) ? part[0] : -INFINITY;
+          }
+        }
+      }
+    }
+    __syncthreads();
+    if (tid == 0 && !*abort_flag) {
+      // Refill the stages the two tiles of this chunk just released.
+      for (int t = 2 * c + kKStages; t < min(nt, 2 * c + kKStages + 2); ++t) issue_k(t);
+    }
+
+    // ---------------------------------------------------------------- C(c-1)
+    if (kPV && c >= 1) {
+      const int pc = c - 1, pcb = pc & 1;
+      const int ns = ctl->n_surv;
+      if (ns > 0) {
+        bool ok = true;
+        for (int s = 0; s < ns; ++s) ok = ok && mbar_wait(&ctl->v_full[s], ctl->surv_par[s], abort_flag);
+        if (warp < GP) {
+          const int g = warp;
+          for (int s = 0; s < ns; ++s) {
+            const int tl = ctl->surv_tile[s] - 2 * pc;
+            float* prow = sP + s * kTile * GP;
+            if (g < G) {
+              const float tm = sTm[(pcb * 2 + tl) * GP + g];
+              const float m_new = fmaxf(m_run, tm);
+              const float alpha = (m_run == -INFINITY) ? 0.f : ex2_approx((m_run - m_new) * sl2);
+              const float mb = (m_new == -INFINITY) ? 0.f : m_new * sl2;
+              const float* sc = SC(pcb, tl, g);
+              float sum = 0.f;
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const int k = lane + 32 * kk;
+                const float pv = ex2_approx(fmaf(sc[k], sl2, -mb));
+                prow[k * GP + g] = pv;
+                sum += pv;
+              }
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+              l_run = alpha * l_run + sum;
+              m_run = m_new;
+              if (lane == 0) sAl[s * GP + g] = alpha;
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) prow[(lane + 32 * kk) * GP + g] = 0.f;
+              if (lane == 0) sAl[s * GP + g] = 1.f;
+            }
+          }
+        }
+        __syncthreads();
+        if (ok) {
+          const int dp = tid % C::kNDP, kg = tid / C::kNDP;
+          for (int s = 0; s < ns; ++s) {
+#pragma unroll
+            for (int g = 0; g < GP; ++g) {
+              const float a = sAl[s * GP + g];
+              acc[g][0] *= a;
+              acc[g][1] *= a;
+            }
+            const int valid = tile_rows(ctl->surv_tile[s]);
+            const uint8_t* vt = sV + s * C::kTileBytes;
+            const float* prow = sP + s * kTile * GP;
+            const int k0 = kg * C::kKPG;
+            const int kend = min(C::kKPG, valid - k0);
+#pragma unroll 4
+            for (int kk = 0; kk < kend; ++kk) {
+              const int k = k0 + kk;
+              const uint32_t w = *reinterpret_cast<const uint32_t*>(vt + k * D * 2 + dp * 4);
+              const float v0 = __uint_as_float(w << 16), v1 = __uint_as_float(w & 0xffff0000u);
+              float pk[GP];
+              if constexpr (GP >= 4) {
+#pragma unroll
+                for (int g4 = 0; g4 < GP; g4 += 4) {
+                  const float4 q4 = *reinterpret_cast<const float4*>(prow + k * GP + g4);
+                  pk[g4] = q4.x; pk[g4 + 1] = q4.y; pk[g4 + 2] = q4.z; pk[g4 + 3] = q4.w;
+                }
+              } else {
+#pragma unroll
+                for (int g = 0; g < GP; ++g) pk[g] = prow[k * GP + g];
+              }
+#pragma unroll
+              for (int g = 0; g < GP; ++g) {
+                acc[g][0] = fmaf(pk[g], v0, acc[g][0]);
+                acc[g][1] = fmaf(pk[g], v1, acc[g][1]);
+              }
+            }
+          }
+        }
+      }
+    }
+
+    // ---------------------------------------------------------------- B(c)
+    if (c < nchunks) {
+      for (int q = warp; q < 2 * G; q += kDecThreads / 32) {
+        const int tl = q / G, g = q - (q / G) * G;
+        if (2 * c + tl < nt) {
+          const float* sc = SC(cb, tl, g);
+          float m = fmaxf(fmaxf(sc[lane], sc[lane + 32]), fmaxf(sc[lane + 64], sc[lane + 96]));
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+          if (lane == 0) sTm[(cb * 2 + tl) * GP + g] = m;
+        }
+      }
+      __syncthreads();
+      if (tid == 0) {
+        int ns = 0;
+        for (int tl = 0; tl < 2 && 2 * c + tl < nt; ++tl) {
+          const int t = 2 * c + tl;
+          float cval = -INFINITY;
+#pragma unroll
+          for (int g = 0; g < GP; ++g) {
+            if (g < G) {
+              const float tm = sTm[(cb * 2 + tl) * GP + g];
+              if (tm != -INFINITY) cval = fmaxf(cval, (mt[g] == -INFINITY) ? INFINITY : tm - mt[g]);
+              mt[g] = fmaxf(mt[g], tm);
+            }
+          }
+          const bool skip = kVote && (cval < p.thr_raw);
+          const long gi = static_cast<long>(bk) * p.nT + j0 + t;
+          if (p.mask != nullptr) p.mask[gi] = skip ? 1 : 0;
+          if (p.margin != nullptr) p.margin[gi] = (cval == INFINITY) ? INFINITY : cval * p.scale;
+          if (skip) {
+            ++skipped;
+          } else if (kPV) {
+            // Batched V fetch of this chunk's survivors (§Kernel-ontwerp).
+            const uint32_t bytes = static_cast<uint32_t>(tile_rows(t)) * D * 2;
+            ctl->surv_tile[ns] = t;
+            ctl->surv_par[ns] = nv_issued[ns] & 1u;
+            if (!*abort_flag) {
+              mbar_arrive_expect_tx(&ctl->v_full[ns], bytes);
+              bulk_load(sV + ns * C::kTileBytes, vbase + static_cast<size_t>(j0 + t) * kTile * D,
+                        bytes, &ctl->v_full[ns]);
+              ++nv_issued[ns];
+            }
+            ++ns;
+          }
+        }
+        ctl->n_surv = ns;
+      }
+    }
+    __syncthreads();
+  }
+
+  // ------------------------------------------------------------------ output
+  if (kPV && !*abort_flag) {
+    if (warp < GP && lane == 0) {
+      sMl[warp * 2] = m_run;
+      sMl[warp * 2 + 1] = l_run;
+    }
+    float* red = reinterpret_cast<float*>(sK);  // every K load has been consumed
+    const int dp = tid % C::kNDP, kg = tid / C::kNDP;
+#pragma unroll
+    for (int g = 0; g < GP; ++g) {
+      red[(kg * GP + g) * D + 2 * dp] = acc[g][0];
+      red[(kg * GP + g) * D + 2 * dp + 1] = acc[g][1];
+    }
+    __syncthreads();
+    for (int idx = tid; idx < G * D; idx += kDecThreads) {
+      const int g = idx / D, e = idx - (idx / D) * D;
+      float sum = 0.f;
+#pragma unroll
+      for (int kg2 = 0; kg2 < C::kNKG; ++kg2) sum += red[(kg2 * GP + g) * D + e];
+      const size_t row = static_cast<size_t>(b) * p.Hq + kvh * G + g;
+      if (p.S == 1) {
+        const float l = sMl[g * 2 + 1];
+        p.o[row * D + e] = __float2bfloat16_rn(l > 0.f ? sum / l : 0.f);
+      } else {
+        float* pr = p.part + (row * p.S + split) * (D + 2);
+        pr[e] = sum;
+        if (e == 0) {
+          const float m = sMl[g * 2];
+          pr[D] = (m == -INFINITY) ? -INFINITY : m * sl2;
+          pr[D + 1] = sMl[g * 2 + 1];
+        }
+      }
+    }
+  }
+  if (tid == 0) {
+    if (p.counts != nullptr) p.counts[static_cast<long>(bk) * p.S + split] = skipped;
+    if (*abort_flag) {
+      // Let in-flight copies land before shared memory is released.
+      for (int s = 0; s < kKStages; ++s)
+        if (nk_issued > s) {
+          const int ik = s + ((nk_issued - 1 - s) / kKStages) * kKStages;
+          mbar_wait(&ctl->k_full[s], (ik / kKStages) & 1, nullptr);
+        }
+      for (int s = 0; s < 2; ++s)
+        if (nv_issued[s] > 0) mbar_wait(&ctl->v_full[s], (nv_issued[s] - 1) & 1, nullptr);
+      report_timeout(p.status);
+    }
+  }
+}
+
+// Log-sum-exp merge of the per-split partial states: one warp per (b, h_q).
+template <int D>
+__global__ void __launch_bounds__(256) decode_merge_kernel(const float* __restrict__ part,
+                                                           __nv_bfloat16* __restrict__ o, int rows,
+                                                           int S) {
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const float* pr = part + static_cast<size_t>(row) * S * (D + 2);
+  float mstar = -INFINITY;
+  for (int s = 0; s < S; ++s) {
+    const float l = pr[s * (D + 2) + D + 1];
+    if (l > 0.f) mstar = fmaxf(mstar, pr[s * (D + 2) + D]);
+  }
+  constexpr int E = D / 32;
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  float L = 0.f;
+  for (int s = 0; s < S; ++s) {
+    const float l = pr[s * (D + 2) + D + 1];
+    if (!(l > 0.f)) continue;
+    const float w = ex2_approx(pr[s * (D + 2) + D] - mstar);
+    L = fmaf(l, w, L);
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = fmaf(pr[s * (D + 2) + lane + 32 * e], w, acc[e]);
+  }
+  const float inv = (L > 0.f) ? 1.f / L : 0.f;
+#pragma unroll
+  for (int e = 0; e < E; ++e) o[static_cast<size_t>(row) * D + lane + 32 * e] = __float2bfloat16_rn(acc[e] * inv);
+}
+
+template <int D, int GP, Mode MODE>
+cudaError_t launch_dec(const DecodeParams& p, cudaStream_t st) {
+  using C = DecodeCfg<D, GP>;
+  auto* fn = decode_kernel<D, GP, MODE>;
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const long ctas = static_cast<long>(p.B) * p.Hkv * p.S;
+  fn<<<dim3(static_cast<unsigned>(ctas)), dim3(kDecThreads), C::kSmemBytes, st>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || MODE == Mode::kCount || p.S == 1) return e;
+  const int rows = p.B * p.Hq;
+  decode_merge_kernel<D><<<dim3((rows + 7) / 8), dim3(256), 0, st>>>(p.part, p.o, rows, p.S);
+  return cudaGetLastError();
+}
+
+template <int D, int GP>
+cudaError_t launch_dec_mode(const DecodeParams& p, Mode mode, cudaStream_t st) {
+  switch (mode) {
+    case Mode::kDense: return launch_dec<D, GP, Mode::kDense>(p, st);
+    case Mode::kSparse: return launch_dec<D, GP, Mode::kSparse>(p, st);
+    default: return launch_dec<D, GP, Mode::kCount>(p, st);
+  }
+}
+
+template <int D>
+cudaError_t launch_dec_g(const DecodeParams& p, Mode mode, cudaStream_t st) {
+  if (p.G <= 1) return launch_dec_mode<D, 1>(p, mode, st);
+  if (p.G <= 2) return launch_dec_mode<D, 2>(p, mode, st);
+  if (p.G <= 4) return launch_dec_mode<D, 4>(p, mode, st);
+  return launch_dec_mode<D, 8>(p, mode, st);
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeParams& p, Mode mode, cudaStream_t st) {
+  return (p.d == 128) ? launch_dec_g<128>(p, mode, st) : launch_dec_g<64>(p, mode, st);
+}
+
+}  // namespace ssattn

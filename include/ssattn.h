@@ -1,0 +1,194 @@
+/*
+ * ssattn -- skip-softmax (BLASST) attention forward for NVIDIA GB300 (sm_103a).
+ *
+ * C ABI.  Plain pointers and sizes only; every device pointer is memory the
+ * caller owns (e.g. a framework tensor's data pointer), and the library
+ * allocates no device memory.  Every compute call is asynchronous on the
+ * caller's stream (`stream` is a cudaStream_t passed as void*, NULL meaning
+ * the legacy default stream); a returned SS_OK means the work was validated
+ * and launched.  Errors found on the device (a bounded wait that expired)
+ * are recorded in a library-wide device status word read by
+ * ss_stream_status().
+ *
+ * The method (cited by page title and section):
+ *   "Skip-Softmax" (vllm-omni design doc):
+ *     §The online-softmax pass -- one streaming pass over 128-key tiles
+ *       keeping the running max m, the denominator l = sum exp(s - m) and the
+ *       numerator O = sum exp(s - m) v, returning O / l;
+ *     §The skip test -- once tile j's scores Q K_j^T * scale are known, the
+ *       tile is skipped when exp(tile_max - running_max) < threshold: no
+ *       exponentials, no P.V accumulation, no contribution to l or O;
+ *     §What this bounds -- Q K^T always runs; the decision is per tile;
+ *     §The threshold -- threshold = factor / seqlen, factor either calibrated
+ *       (factor = a * exp(b * target_sparsity)) or direct.
+ *   "BLASST: Dynamic BLocked Attention Sparsity via Softmax Thresholding"
+ *   (summary of arXiv 2512.12087):
+ *     §Methodologie -- the test in log form (local max - running max < ln
+ *       lambda); in decode a skipped tile's V block is never loaded;
+ *     §Calibratie -- lambda = a / L; an automated procedure picks a so that
+ *       a fixed fraction of tiles is skipped at any context length;
+ *     §Kernel-ontwerp -- prefill skips softmax and P.V MMA, decode skips V
+ *       loads with batched loading of surviving tiles.
+ *
+ * Conventions shared by all entry points:
+ *   - q, k, v, o are bf16, contiguous, 16-byte aligned.  Prefill layouts:
+ *     q, o [B, Hq, Lq, d]; k, v [B, Hkv, Lk, d].  Decode: q, o [B, Hq, d],
+ *     k, v [B, Hkv, Lk, d].
+ *   - d is 64 or 128.  Hq must be a multiple of Hkv; query head h reads KV
+ *     head h / (Hq / Hkv) (MHA: Hkv = Hq, GQA, MQA: Hkv = 1).
+ *   - Key tiles and prefill query blocks are 128 wide; Lq and Lk need not be
+ *     multiples of 128 (tails are masked).
+ *   - Causal masking is bottom-right aligned: key k is visible to query row r
+ *     iff k <= r + (Lk - Lq).
+ *   - lambda in [0, 1]; lambda = 0 runs the dense path (no vote at all).
+ *     A tile is skipped iff every query row of the block (decode: every query
+ *     head sharing the KV head) has exp(scale*(tile_max - running_max)) <
+ *     lambda, the running max being the maximum over the earlier tiles of the
+ *     same pass (decode: the same split).  A row with no visible key in the
+ *     tile does not veto.  The first tile of a pass is never skipped.
+ */
+#ifndef SSATTN_H
+#define SSATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SS_OK = 0,
+  SS_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad shape, lambda or scale */
+  SS_ERR_UNSUPPORTED = 2,  /* d not in {64,128}, or the current device is not sm_103 */
+  SS_ERR_CUDA = 3,         /* a CUDA runtime call failed (launch, copy, sync) */
+  SS_ERR_TIMEOUT = 4,      /* a kernel's bounded wait expired (logic error; reported, not hung) */
+  SS_ERR_WORKSPACE = 5     /* decode workspace missing or too small */
+} ss_status;
+
+/* Optional debug / calibration outputs, all device pointers, all nullable. */
+typedef struct {
+  /* One byte per (unit, key tile): 0 kept, 1 skipped, 2 not evaluated
+     (causal tiles past the diagonal).  Prefill: [B*Hq*ceil(Lq/128)][nT];
+     decode: [B*Hkv][nT] with tiles indexed globally. */
+  uint8_t* skip_mask;
+  /* Vote statistic c_j = max over rows of scale*(tile_max - running_max) in
+     natural-log units, same indexing as skip_mask; +INF when some row has no
+     running max yet, NAN when not evaluated.  The tile is skipped iff
+     c_j < ln(lambda). */
+  float* vote_margin;
+  /* Nonzero: compute scores, the vote and the counters only -- no
+     exponentials, no P.V, no V loads, no output written (o may be NULL).
+     Decisions equal those of the full pass: a skipped tile never raises the
+     running max when lambda <= 1. */
+  int count_only;
+} ss_debug_opts;
+
+/*
+ * Prefill forward (all §8 prefill steps: TMA staging, Q K^T on tcgen05,
+ * mask + tile max, skip vote, online softmax on kept tiles, P.V on tcgen05,
+ * O / l epilogue).
+ *   skip_counts: nullable device buffer [B*Hq*ceil(Lq/128)], one uint32 per
+ *   (b, h_q, query block) = skipped tiles of that unit; overwritten.
+ * Returns SS_OK, SS_ERR_INVALID_ARG, SS_ERR_UNSUPPORTED or SS_ERR_CUDA.
+ */
+ss_status ss_attn_prefill(const void* q, const void* k, const void* v, void* o, int B, int Hq,
+                          int Hkv, int Lq, int Lk, int d, float scale, int causal, float lambda,
+                          uint32_t* skip_counts, void* stream);
+
+ss_status ss_attn_prefill_ex(const void* q, const void* k, const void* v, void* o, int B,
+                             int Hq, int Hkv, int Lq, int Lk, int d, float scale, int causal,
+                             float lambda, uint32_t* skip_counts, const ss_debug_opts* dbg,
+                             void* stream);
+
+/*
+ * Bytes of device workspace ss_attn_decode needs for the per-split partial
+ * states (m, l, O in fp32): 0 when num_kv_splits == 1.
+ */
+size_t ss_attn_decode_workspace_size(int B, int Hq, int d, int num_kv_splits);
+
+/*
+ * Split-KV decode forward (one query token per sequence).  The nT =
+ * ceil(Lk/128) key tiles are cut into num_kv_splits contiguous ranges of
+ * ceil(nT/num_kv_splits) tiles; each range runs its own online pass (its
+ * first tile is always kept), streams all of its K, loads V only for kept
+ * tiles, and writes a partial (m, l, O); a second kernel merges the
+ * partials by log-sum-exp into bf16 o.
+ *   skip_counts: nullable device buffer [B*Hkv*num_kv_splits] (skipped tiles
+ *     per (sequence, KV head, split)); overwritten.
+ *   workspace: device buffer of at least
+ *     ss_attn_decode_workspace_size(B, Hq, d, num_kv_splits) bytes, 16-byte
+ *     aligned (may be NULL when that size is 0); contents need not be
+ *     initialised and are clobbered.
+ * Returns SS_OK, SS_ERR_INVALID_ARG, SS_ERR_UNSUPPORTED, SS_ERR_WORKSPACE or
+ * SS_ERR_CUDA.
+ */
+ss_status ss_attn_decode(const void* q, const void* k_cache, const void* v_cache, void* o, int B,
+                         int Hq, int Hkv, int Lk, int d, float scale, float lambda,
+                         int num_kv_splits, uint32_t* skip_counts, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
+ss_status ss_attn_decode_ex(const void* q, const void* k_cache, const void* v_cache, void* o,
+                            int B, int Hq, int Hkv, int Lk, int d, float scale, float lambda,
+                            int num_kv_splits, uint32_t* skip_counts, void* workspace,
+                            size_t workspace_bytes, const ss_debug_opts* dbg, void* stream);
+
+/* A calibration problem: the inputs the threshold is fitted on. */
+typedef enum { SS_PREFILL = 0, SS_DECODE = 1 } ss_kind;
+typedef struct {
+  ss_kind kind;
+  const void* q;
+  const void* k;
+  const void* v;
+  int B, Hq, Hkv;
+  int Lq;          /* prefill only */
+  int Lk;          /* also the L in lambda = a / L */
+  int d;
+  float scale;
+  int causal;      /* prefill only */
+  int num_kv_splits; /* decode only */
+  /* Device buffer for the per-unit counters, sized as the matching call's
+     skip_counts (prefill: B*Hq*ceil(Lq/128); decode: B*Hkv*num_kv_splits). */
+  uint32_t* skip_counts;
+  void* stream;
+} ss_problem;
+
+/*
+ * Automated calibration (BLASST summary, §Calibratie): finds a with
+ * lambda = a / Lk such that the fraction of skipped tiles over all evaluated
+ * (unit, tile) pairs of `p` is round(target*N)/N, N the number of evaluated
+ * tiles.  It bisects on ln a with count-only launches, reading the skipped-
+ * tile counters back after each, and returns the log-midpoint of the
+ * interval of a that hits the target count (the widest margin), clamped to
+ * lambda <= 1.  When the target is not reachable under lambda <= 1 it
+ * returns the a closest to it.  Synchronises p->stream.
+ *   a_out: the fitted a (0 when the target rounds to zero skipped tiles).
+ *   achieved_out (nullable): skipped / evaluated at the returned a.
+ */
+ss_status ss_calibrate(const ss_problem* p, float target_sparsity, float* a_out,
+                       float* achieved_out);
+
+/*
+ * Least-squares fit of ln a = ln A + B * s over n >= 2 points with a > 0
+ * ("Skip-Softmax", §The threshold: factor = a * exp(b * target_sparsity);
+ * the fitted pair is returned as (A, B)).  Host only.
+ */
+ss_status ss_fit_factor(const float* s, const float* a, int n, float* A_out, float* B_out);
+
+/* lambda = A * exp(B * s) / L (§The threshold: threshold = factor / seqlen). */
+float ss_lambda(float A, float B, float s, int L);
+
+/* Static description of a status code. */
+const char* ss_status_string(ss_status st);
+
+/*
+ * Synchronise `stream`, then return and clear the device status word:
+ * SS_ERR_TIMEOUT if any kernel since the last call gave up a bounded wait,
+ * SS_ERR_CUDA if the synchronisation failed, SS_OK otherwise.
+ */
+ss_status ss_stream_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SSATTN_H */

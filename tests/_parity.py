@@ -1,0 +1,193 @@
+"""Shared comparison logic for the GPU-vs-oracle parity tests.
+
+Acceptance (per unit):
+* skip decisions agree bit-exactly except on "near-margin" tiles, where the
+  oracle's vote statistic c_j lies within 1e-2 (natural log) of ln(lambda);
+  those disagreements are counted and returned, not failed;
+* skipped-tile counts agree exactly on units whose decisions all agree, and
+  always equal the number of skipped tiles in the GPU's own mask;
+* outputs agree within max-abs 2e-2 and mean-abs 2e-3 (bf16 output), both
+  against the oracle with its own decisions (units without disagreement) and
+  against the oracle re-run under the GPU's decisions (arithmetic only).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+import oracle
+from block_sparse_attention_sm_gb300 import capi, synth
+
+MAX_ABS = 2e-2
+MEAN_ABS = 2e-3
+NEAR_MARGIN = 1e-2
+TILE = 128
+
+
+def _ln(lam):
+    return math.log(lam) if lam > 0 else -math.inf
+
+
+def compare_decisions(gpu_mask, gpu_margin, orc_mask, orc_margin, lam):
+    """Returns (n_disagree, per-row disagreement flags); asserts the rest."""
+    ln_lam = _ln(lam)
+    gm = gpu_mask.astype(np.int64)
+    om = orc_mask.astype(np.int64)
+    # "not evaluated" must agree exactly (pure index arithmetic).
+    assert np.array_equal(gm == 2, om == 2), "evaluated-tile sets differ"
+    dis = gm != om
+    near = np.abs(orc_margin - ln_lam) < NEAR_MARGIN
+    bad = dis & ~near
+    assert not bad.any(), (
+        f"{int(bad.sum())} decision(s) disagree outside the {NEAR_MARGIN} log margin; "
+        f"first at {np.argwhere(bad)[0].tolist()} margin {orc_margin[bad][0]} ln(lam) {ln_lam}")
+    # vote statistic itself: +inf where the oracle has +inf, close elsewhere
+    ev = om != 2
+    inf_o = np.isposinf(orc_margin) & ev
+    assert np.array_equal(np.isposinf(gpu_margin) & ev, inf_o), "first-tile (+inf) margins differ"
+    fin = ev & ~inf_o
+    if fin.any():
+        err = np.abs(gpu_margin[fin].astype(np.float64) - orc_margin[fin])
+        assert err.max() <= 2e-2 + 2e-4 * np.abs(orc_margin[fin]).max(), f"margin error {err.max()}"
+    return int(dis.sum()), dis.any(axis=-1)
+
+
+def check_output(o_gpu, o_ref, what=""):
+    o_gpu = o_gpu.astype(np.float64)
+    err = np.abs(o_gpu - o_ref)
+    mx, mean = float(err.max(initial=0.0)), float(err.mean()) if err.size else 0.0
+    assert mx <= MAX_ABS and mean <= MEAN_ABS, f"{what}: max-abs {mx:.3e} mean-abs {mean:.3e}"
+    return mx, mean
+
+
+def gpu_prefill_all(q, k, v, scale, causal, lam):
+    """Bench-configuration call (plain entry point) plus the debug call."""
+    B, Hq, Lq, d = q.shape
+    _, Hkv, Lk, _ = k.shape
+    nqb, nT = -(-Lq // TILE), -(-Lk // TILE)
+    n_units = B * Hq * nqb
+    dev = q.device
+    o = torch.empty_like(q)
+    counts = torch.full((n_units,), -1, dtype=torch.int32, device=dev)
+    st = capi.ss_attn_prefill(q, k, v, o, B, Hq, Hkv, Lq, Lk, d, scale, causal, lam, counts)
+    assert st == capi.SS_OK, capi.ss_status_string(st)
+    o2 = torch.empty_like(q)
+    counts2 = torch.full((n_units,), -1, dtype=torch.int32, device=dev)
+    mask = torch.full((n_units, nT), 7, dtype=torch.uint8, device=dev)
+    margin = torch.full((n_units, nT), 12345.0, dtype=torch.float32, device=dev)
+    st = capi.ss_attn_prefill_ex(q, k, v, o2, B, Hq, Hkv, Lq, Lk, d, scale, causal, lam, counts2,
+                                 mask, margin)
+    assert st == capi.SS_OK, capi.ss_status_string(st)
+    assert capi.ss_stream_status() == capi.SS_OK
+    torch.cuda.synchronize()
+    # the debug outputs do not change the result
+    assert torch.equal(o, o2) and torch.equal(counts, counts2)
+    return o, counts, mask, margin
+
+
+def check_prefill(q, k, v, *, scale, causal, lam, units=None):
+    """Parity of one prefill launch; `units` = list of (b, h, qb) or None (all).
+
+    Returns the number of near-margin disagreements."""
+    B, Hq, Lq, d = q.shape
+    _, Hkv, Lk, _ = k.shape
+    G = Hq // Hkv
+    nqb = -(-Lq // TILE)
+    o, counts, mask, margin = gpu_prefill_all(q, k, v, scale, causal, lam)
+    if units is None:
+        units = [(b, h, qb) for b in range(B) for h in range(Hq) for qb in range(nqb)]
+    by_head = {}
+    for (b, h, qb) in units:
+        by_head.setdefault((b, h), []).append(qb)
+    n_dis = 0
+    counts_h = counts.cpu().numpy()
+    mask_h = mask.cpu().numpy()
+    margin_h = margin.cpu().numpy()
+    for (b, h), qbs in sorted(by_head.items()):
+        kvh = h // G
+        qs, ks, vs = q[b:b + 1, h:h + 1], k[b:b + 1, kvh:kvh + 1], v[b:b + 1, kvh:kvh + 1]
+        ref = oracle.prefill(qs, ks, vs, scale=scale, causal=causal, lam=lam, units=qbs)
+        gids = [(b * Hq + h) * nqb + qb for qb in qbs]
+        gmask, gmargin = mask_h[gids], margin_h[gids]
+        nd, row_dis = compare_decisions(gmask, gmargin, ref.mask, ref.margin, lam)
+        n_dis += nd
+        np.testing.assert_array_equal(counts_h[gids], (gmask == 1).sum(axis=1))
+        for i, qb in enumerate(qbs):
+            if not row_dis[i]:
+                assert counts_h[gids[i]] == ref.counts[i]
+        over = oracle.prefill(qs, ks, vs, scale=scale, causal=causal, lam=lam, units=qbs,
+                              mask_override=(gmask == 1).astype(np.uint8))
+        og = o[b, h].float().cpu().numpy()
+        for i, qb in enumerate(qbs):
+            r0, r1 = qb * TILE, min(Lq, qb * TILE + TILE)
+            check_output(og[r0:r1], over.o[i, : r1 - r0], f"unit {(b, h, qb)} under GPU mask")
+            if not row_dis[i]:
+                check_output(og[r0:r1], ref.o[i, : r1 - r0], f"unit {(b, h, qb)}")
+    return n_dis
+
+
+def check_decode(q, k, v, *, scale, lam, num_splits, units=None):
+    """Parity of one decode launch; `units` = list of b*Hkv + kvh (None: all)."""
+    B, Hq, d = q.shape
+    _, Hkv, Lk, _ = k.shape
+    G = Hq // Hkv
+    nT = -(-Lk // TILE)
+    S = num_splits
+    dev = q.device
+    ws_n = capi.ss_attn_decode_workspace_size(B, Hq, d, S)
+    ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=dev)
+    o = torch.empty_like(q)
+    counts = torch.full((B * Hkv * S,), -1, dtype=torch.int32, device=dev)
+    st = capi.ss_attn_decode(q, k, v, o, B, Hq, Hkv, Lk, d, scale, lam, S, counts, ws, ws_n)
+    assert st == capi.SS_OK, capi.ss_status_string(st)
+    o2 = torch.empty_like(q)
+    counts2 = torch.full_like(counts, -1)
+    mask = torch.full((B * Hkv, nT), 7, dtype=torch.uint8, device=dev)
+    margin = torch.full((B * Hkv, nT), 12345.0, dtype=torch.float32, device=dev)
+    st = capi.ss_attn_decode_ex(q, k, v, o2, B, Hq, Hkv, Lk, d, scale, lam, S, counts2, ws, ws_n,
+                                mask, margin)
+    assert st == capi.SS_OK, capi.ss_status_string(st)
+    assert capi.ss_stream_status() == capi.SS_OK
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2) and torch.equal(counts, counts2)
+    if units is None:
+        units = list(range(B * Hkv))
+    units = sorted(units)
+    ch = counts.cpu().numpy().reshape(B * Hkv, S)
+    mh = mask.cpu().numpy()
+    gh = margin.cpu().numpy()
+    og = o.float().cpu().numpy()
+    T = -(-nT // S)
+    n_dis = 0
+    for u in units:
+        b, kvh = divmod(u, Hkv)
+        qs = q[b:b + 1, kvh * G:(kvh + 1) * G]
+        ks, vs = k[b:b + 1, kvh:kvh + 1], v[b:b + 1, kvh:kvh + 1]
+        ref = oracle.decode(qs, ks, vs, scale=scale, lam=lam, num_splits=S)
+        nd, row_dis = compare_decisions(mh[u:u + 1], gh[u:u + 1], ref.mask, ref.margin, lam)
+        n_dis += nd
+        for sp in range(S):
+            tiles = range(sp * T, min(nT, sp * T + T))
+            gsk = int((mh[u, list(tiles)] == 1).sum()) if len(tiles) else 0
+            assert ch[u, sp] == gsk
+            if not row_dis[0]:
+                assert ch[u, sp] == ref.counts[0, sp]
+        over = oracle.decode(qs, ks, vs, scale=scale, lam=lam, num_splits=S,
+                             mask_override=(mh[u:u + 1] == 1).astype(np.uint8))
+        check_output(og[b, kvh * G:(kvh + 1) * G], over.o[0], f"decode unit {u} under GPU mask")
+        if not row_dis[0]:
+            check_output(og[b, kvh * G:(kvh + 1) * G], ref.o[0], f"decode unit {u}")
+    return n_dis
+
+
+def hot_prefill(B, Hq, Hkv, Lq, Lk, d, frac=0.2, seed=0, per_head_u=True):
+    inp = synth.prefill_inputs(B=B, Hq=Hq, Hkv=Hkv, Lq=Lq, Lk=Lk, d=d, hot_frac=frac, seed=seed,
+                               per_head_u=per_head_u, device="cuda")
+    return inp
+
+
+def hot_decode(B, Hq, Hkv, Lk, d, frac=0.2, seed=0):
+    return synth.decode_inputs(B=B, Hq=Hq, Hkv=Hkv, Lk=Lk, d=d, hot_frac=frac, seed=seed,
+                               device="cuda")

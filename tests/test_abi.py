@@ -1,0 +1,119 @@
+"""The C-ABI library loads and exports what include/ssattn.h declares (CPU).
+
+No compute call reaches a GPU here: only host-side logic (argument
+validation that rejects before any device work, the factor fit, lambda,
+status strings)."""
+import ctypes
+import math
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ssattn.h")
+
+
+@pytest.fixture(scope="module")
+def capi():
+    import block_sparse_attention_sm_gb300 as ss
+    from block_sparse_attention_sm_gb300 import capi
+
+    ss.build()
+    capi.load()
+    return capi
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ss_[a-z_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(capi):
+    decl = declared_functions()
+    assert len(decl) >= 10
+    out = subprocess.run(["nm", "-D", "--defined-only", capi.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\s[TW]\s+(\S+)$", out, flags=re.M))
+    missing = [f for f in decl if f not in exported]
+    assert not missing, f"declared but not exported: {missing}"
+    assert set(capi.EXPORTS) == set(decl)
+    for f in decl:
+        assert hasattr(capi.load(), f)
+
+
+def test_status_strings(capi):
+    for st in range(6):
+        assert capi.ss_status_string(st)
+    assert "invalid" in capi.ss_status_string(capi.SS_ERR_INVALID_ARG)
+
+
+def test_lambda_and_fit(capi):
+    # §The threshold: threshold = factor / seqlen, factor = A exp(B s)
+    assert math.isclose(capi.ss_lambda(2.0, 1.5, 0.7, 4096), 2.0 * math.exp(1.05) / 4096,
+                        rel_tol=1e-6)
+    s = [0.5, 0.7, 0.9]
+    a = [3.0 * math.exp(2.0 * x) for x in s]
+    st, A, B = capi.ss_fit_factor(s, a)
+    assert st == capi.SS_OK
+    assert math.isclose(A, 3.0, rel_tol=1e-5) and math.isclose(B, 2.0, rel_tol=1e-5)
+    assert capi.ss_fit_factor([0.5], [1.0])[0] == capi.SS_ERR_INVALID_ARG
+    assert capi.ss_fit_factor([0.5, 0.6], [1.0, -1.0])[0] == capi.SS_ERR_INVALID_ARG
+
+
+FAKE = 1 << 20  # a 16-byte-aligned non-null address; never dereferenced here
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(q=None), "SS_ERR_INVALID_ARG"),
+    (dict(q=FAKE + 8), "SS_ERR_INVALID_ARG"),          # misaligned
+    (dict(Lq=0), "SS_ERR_INVALID_ARG"),                # empty input
+    (dict(B=0), "SS_ERR_INVALID_ARG"),
+    (dict(Hq=3, Hkv=2), "SS_ERR_INVALID_ARG"),         # Hq % Hkv != 0
+    (dict(lam=1.5), "SS_ERR_INVALID_ARG"),
+    (dict(lam=float("nan")), "SS_ERR_INVALID_ARG"),
+    (dict(lam=-0.1), "SS_ERR_INVALID_ARG"),
+    (dict(scale=0.0), "SS_ERR_INVALID_ARG"),
+    (dict(d=96), "SS_ERR_UNSUPPORTED"),
+])
+def test_prefill_rejects_before_launch(capi, kw, expect):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, B=1, Hq=2, Hkv=1, Lq=128, Lk=128, d=128,
+                scale=0.1, causal=0, lam=0.01)
+    args.update(kw)
+    st = capi.ss_attn_prefill(args["q"], args["k"], args["v"], args["o"], args["B"], args["Hq"],
+                              args["Hkv"], args["Lq"], args["Lk"], args["d"], args["scale"],
+                              args["causal"], args["lam"], None, 0)
+    assert st == getattr(capi, expect)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(S=0), "SS_ERR_INVALID_ARG"),
+    (dict(Lk=0), "SS_ERR_INVALID_ARG"),
+    (dict(Hq=32, Hkv=2), "SS_ERR_UNSUPPORTED"),       # vote group > 8
+    (dict(S=4, ws=None), "SS_ERR_WORKSPACE"),
+    (dict(S=4, ws_bytes=16), "SS_ERR_WORKSPACE"),
+])
+def test_decode_rejects_before_launch(capi, kw, expect):
+    args = dict(B=2, Hq=8, Hkv=2, Lk=1000, d=128, S=1, ws=FAKE, ws_bytes=1 << 30)
+    args.update(kw)
+    st = capi.ss_attn_decode(FAKE, FAKE, FAKE, FAKE, args["B"], args["Hq"], args["Hkv"],
+                             args["Lk"], args["d"], 0.1, 0.01, args["S"], None, args["ws"],
+                             args["ws_bytes"], 0)
+    assert st == getattr(capi, expect)
+
+
+def test_workspace_size(capi):
+    assert capi.ss_attn_decode_workspace_size(64, 32, 128, 1) == 0
+    assert capi.ss_attn_decode_workspace_size(64, 32, 128, 8) == 64 * 32 * 8 * 130 * 4
+
+
+def test_product_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "block_sparse_attention_sm_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "oracle.h" not in text, f

@@ -1,0 +1,69 @@
+"""Split-KV decode kernel vs the fp64 oracle (GPU)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import block_sparse_attention_sm_gb300 as ss
+    import oracle
+
+    ss.build()
+    oracle.build()
+    assert torch.cuda.is_available()
+
+
+SHAPES = [
+    # B, Hq, Hkv, Lk, d, splits
+    (3, 8, 2, 1000, 128, 1),
+    (3, 8, 2, 1000, 128, 3),    # splits that do not divide the 8 tiles
+    (2, 32, 8, 4096, 128, 8),
+    (2, 4, 4, 777, 64, 2),      # MHA (G = 1), d = 64
+    (1, 8, 1, 2000, 128, 16),   # G = 8 (MQA with 8 query heads); one split per tile
+    (2, 6, 2, 1500, 64, 4),     # G = 3 (padded vote group)
+    (1, 4, 1, 100, 128, 1),     # one partial tile
+    (1, 4, 1, 300, 128, 8),     # more splits than tiles: empty splits
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+@pytest.mark.parametrize("a", [0.0, 1.0, 8.0])
+def test_decode_shapes(shape, a):
+    from _parity import check_decode, hot_decode
+
+    B, Hq, Hkv, Lk, d, S = shape
+    inp = hot_decode(B, Hq, Hkv, Lk, d, frac=0.2, seed=4)
+    check_decode(inp.q, inp.k, inp.v, scale=1.0 / math.sqrt(d), lam=min(1.0, a / Lk),
+                 num_splits=S)
+
+
+def test_decode_random_scores():
+    from _parity import check_decode
+
+    g = torch.Generator(device="cuda").manual_seed(9)
+    q = torch.randn(4, 8, 128, device="cuda", generator=g).to(torch.bfloat16)
+    k = torch.randn(4, 2, 3000, 128, device="cuda", generator=g).to(torch.bfloat16)
+    v = torch.randn(4, 2, 3000, 128, device="cuda", generator=g).to(torch.bfloat16)
+    for lam in (0.2, 0.6, 1.0):
+        check_decode(q, k, v, scale=128 ** -0.5, lam=lam, num_splits=5)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("workload,a", [("llama_decode_32k", 2.0), ("long_decode_128k", 4.0)])
+def test_full_size_sampled(workload, a):
+    """Full-size decode in the bench's launch configuration; the oracle checks
+    sampled (sequence, KV head) units in full (every split)."""
+    from _parity import check_decode
+    from block_sparse_attention_sm_gb300 import synth
+
+    inp, cfg = synth.make(workload, seed=0, device="cuda")
+    rng = np.random.default_rng(3)
+    n = cfg["B"] * cfg["Hkv"]
+    units = sorted({0, n - 1, *rng.choice(n, size=6, replace=False).tolist()})
+    check_decode(inp.q, inp.k, inp.v, scale=cfg["scale"], lam=a / cfg["Lk"],
+                 num_splits=cfg["num_splits"], units=units)
