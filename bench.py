@@ -140,7 +140,9 @@ def run_native(args):
     peaks = _peaks()
 
     # ---------------------------------------------------------------- inputs
-    pin, pcfg = synth.make(PREFILL, seed=rank, device=dev)
+    pin, pcfg = synth.make(PREFILL, seed=rank, device=dev,
+                           **({"Hq": args.prefill_heads, "Hkv": args.prefill_heads}
+                              if args.prefill_heads else {}))
     q, k, v = pin.q, pin.k, pin.v
     B, Hq, Lq, d = q.shape
     Hkv, Lk = k.shape[1], k.shape[2]
@@ -150,7 +152,8 @@ def run_native(args):
     o = torch.empty_like(q)
     p_cnt = torch.zeros(p_units, dtype=torch.int32, device=dev)
 
-    din, dcfg = synth.make(DECODE, seed=rank, device=dev)
+    din, dcfg = synth.make(DECODE, seed=rank, device=dev,
+                           **({"B": args.decode_batch} if args.decode_batch else {}))
     dq, dk, dv = din.q, din.k, din.v
     dB, dHq, dd = dq.shape
     dHkv, dLk = dk.shape[1], dk.shape[2]
@@ -225,6 +228,9 @@ def run_native(args):
     ms_d = sum(td) / len(td)
     ms_step = ms_p + ms_d
 
+    if args.profile:
+        # profiling run (under ncu): no extras, no JSON line
+        return
     # dense (lambda = 0) path of the same library, same inputs, same protocol
     tpd, tdd = timed_loop(0.0, 0.0, max(5, args.steps // 4), 2)
     ms_p0 = sum(tpd) / len(tpd)
@@ -456,6 +462,12 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", action="store_true",
+                    help="run calibration + the timed loop only (for ncu); prints nothing")
+    ap.add_argument("--prefill-heads", type=int, default=0,
+                    help="profiling: shrink the prefill workload to this many heads")
+    ap.add_argument("--decode-batch", type=int, default=0,
+                    help="profiling: shrink the decode workload to this many sequences")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -274,8 +274,9 @@ __global__ void __launch_bounds__(192, 1)
       }
 
       // Skip vote: every row must pass exp(scale*(tile_max - m)) < lambda.
+      // (The dense path runs the same reduction only to report margins.)
       bool skip = false;
-      if constexpr (kVote) {
+      if (kVote || p.margin != nullptr) {
         float c_r = -INFINITY;  // a row with no visible key does not veto
         if (tmax != -INFINITY) c_r = (m_true == -INFINITY) ? INFINITY : tmax - m_true;
         const bool warp_pass = __all_sync(0xffffffffu, c_r < p.thr_raw);
@@ -298,7 +299,7 @@ __global__ void __launch_bounds__(192, 1)
           break;
         }
         const volatile int* vv = ctl->verdict[vb];
-        skip = vv[0] && vv[1] && vv[2] && vv[3];
+        skip = kVote && vv[0] && vv[1] && vv[2] && vv[3];
         if (tid == 0 && p.margin != nullptr) {
           const volatile float* rr = ctl->red[vb];
           const float cmax = fmaxf(fmaxf(rr[0], rr[1]), fmaxf(rr[2], rr[3]));
