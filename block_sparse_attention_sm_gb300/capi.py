@@ -19,7 +19,7 @@ SS_PREFILL, SS_DECODE = 0, 1
 
 EXPORTS = (
     "ss_attn_prefill", "ss_attn_prefill_ex", "ss_attn_decode_workspace_size", "ss_attn_decode",
-    "ss_attn_decode_ex", "ss_calibrate", "ss_fit_factor", "ss_lambda", "ss_status_string",
+    "ss_attn_decode_ex", "ss_attn_decode_noalloc", "ss_calibrate", "ss_fit_factor", "ss_lambda", "ss_status_string",
     "ss_stream_status",
 )
 
@@ -63,6 +63,7 @@ def load() -> ctypes.CDLL:
     dec = [P, P, P, P, I, I, I, I, I, F, F, I, P, P, U]
     lib.ss_attn_decode.argtypes = dec + [P]
     lib.ss_attn_decode_ex.argtypes = dec + [ctypes.POINTER(ss_debug_opts), P]
+    lib.ss_attn_decode_noalloc.argtypes = [P, P, P, P, I, I, I, I, I, F, F, I, P, P]
     lib.ss_attn_decode_workspace_size.argtypes = [I, I, I, I]
     lib.ss_attn_decode_workspace_size.restype = U
     lib.ss_calibrate.argtypes = [ctypes.POINTER(ss_problem), F, ctypes.POINTER(F), ctypes.POINTER(F)]
@@ -74,7 +75,7 @@ def load() -> ctypes.CDLL:
     lib.ss_status_string.restype = ctypes.c_char_p
     lib.ss_stream_status.argtypes = [P]
     for name in ("ss_attn_prefill", "ss_attn_prefill_ex", "ss_attn_decode", "ss_attn_decode_ex",
-                 "ss_calibrate", "ss_fit_factor", "ss_stream_status"):
+                 "ss_attn_decode_noalloc", "ss_calibrate", "ss_fit_factor", "ss_stream_status"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -141,6 +142,17 @@ def ss_attn_decode_ex(q, k_cache, v_cache, o, B, Hq, Hkv, Lk, d, scale, lam, num
                                     Lk, d, float(scale), float(lam), int(num_kv_splits),
                                     _ptr(skip_counts), _ptr(workspace), int(workspace_bytes),
                                     ctypes.byref(dbg), _stream(stream))
+
+
+def ss_attn_decode_noalloc(q, k_cache, v_cache, o, B, Hq, Hkv, Lk, d, scale, lam, num_kv_splits,
+                           skip_counts=None, stream=None) -> int:
+    """Decode without a workspace (partials in the library's static device array)."""
+    return load().ss_attn_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), B, Hq,
+                                         Hkv, Lk, d, float(scale), float(lam), int(num_kv_splits),
+                                         _ptr(skip_counts), _stream(stream))
+
+
+SS_DECODE_STATIC_SCRATCH_BYTES = 16 << 20
 
 
 def ss_calibrate(problem: ss_problem, target_sparsity: float):

@@ -218,6 +218,35 @@ long counter_len(const ss_problem& p) {
 }  // namespace
 }  // namespace ssattn
 
+// Partial states of ss_attn_decode_noalloc: module memory of this library,
+// present on every device that loads it, never allocated at run time.
+static __device__ __align__(256) unsigned char g_decode_scratch[SS_DECODE_STATIC_SCRATCH_BYTES];
+
+namespace ssattn {
+namespace {
+
+// Device address of g_decode_scratch on the current device.  Host code only
+// holds a stand-in for the array, so the address is looked up once per
+// device (with that device current) and cached.
+void* decode_scratch_ptr() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return nullptr;
+  static std::mutex mu;
+  static std::vector<void*> ptrs;
+  std::lock_guard<std::mutex> lock(mu);
+  if (static_cast<int>(ptrs.size()) <= dev) ptrs.resize(dev + 1, nullptr);
+  if (ptrs[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_decode_scratch) != cudaSuccess || ptr == nullptr)
+      return nullptr;
+    ptrs[dev] = ptr;
+  }
+  return ptrs[dev];
+}
+
+}  // namespace
+}  // namespace ssattn
+
 using namespace ssattn;
 
 extern "C" {
@@ -260,6 +289,21 @@ ss_status ss_attn_decode(const void* q, const void* k_cache, const void* v_cache
                          size_t workspace_bytes, void* stream) {
   return ss_attn_decode_ex(q, k_cache, v_cache, o, B, Hq, Hkv, Lk, d, scale, lambda,
                            num_kv_splits, skip_counts, workspace, workspace_bytes, nullptr, stream);
+}
+
+ss_status ss_attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                 void* o, int B, int Hq, int Hkv, int Lk, int d, float scale,
+                                 float lambda, int num_kv_splits, uint32_t* skip_counts,
+                                 void* stream) {
+  if (!lambda_ok(lambda)) return SS_ERR_INVALID_ARG;
+  const size_t need = decode_ws(B, Hq, d, num_kv_splits);
+  if (need > SS_DECODE_STATIC_SCRATCH_BYTES) return SS_ERR_WORKSPACE;
+  void* ws = nullptr;
+  if (need > 0 && (ws = decode_scratch_ptr()) == nullptr) return SS_ERR_CUDA;
+  const bool dense = lambda == 0.f;
+  const float thr = dense ? -INFINITY : threshold_raw(std::log(static_cast<double>(lambda)), scale);
+  return decode_impl(q, k_cache, v_cache, o, B, Hq, Hkv, Lk, d, scale, dense, thr, num_kv_splits,
+                     skip_counts, ws, SS_DECODE_STATIC_SCRATCH_BYTES, nullptr, stream);
 }
 
 ss_status ss_calibrate(const ss_problem* p, float target_sparsity, float* a_out,

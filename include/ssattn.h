@@ -133,6 +133,40 @@ ss_status ss_attn_decode_ex(const void* q, const void* k_cache, const void* v_ca
                             int num_kv_splits, uint32_t* skip_counts, void* workspace,
                             size_t workspace_bytes, const ss_debug_opts* dbg, void* stream);
 
+/*
+ * Decode for callers that cannot allocate device memory.  The pages have no
+ * counterpart to this entry point; it exists for users of this library, not
+ * for the method.
+ *
+ * Some callers of a decode step are handed their input and output buffers
+ * and nothing else -- a kernel plugin inside an inference engine that owns
+ * all device memory, or a latency-critical serving loop that must not call
+ * cudaMalloc (an allocation can synchronise the device and may fail under
+ * memory pressure).  They cannot provide ss_attn_decode's workspace.  This
+ * variant runs the same kernels as ss_attn_decode, but keeps the per-split
+ * partial states in a fixed device array that is part of the library itself
+ * (SS_DECODE_STATIC_SCRATCH_BYTES, held by every GPU that loads the library
+ * until the process exits).  It calls no cudaMalloc, cudaFree or other
+ * allocating routine.
+ *
+ * Arguments, layouts and results are those of ss_attn_decode without the
+ * workspace.  Calls whose partials need more than
+ * SS_DECODE_STATIC_SCRATCH_BYTES (B*Hq*num_kv_splits*(d+2)*4 bytes when
+ * num_kv_splits > 1) return SS_ERR_WORKSPACE without launching anything.
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture on that device.  Every call on a device shares the one array and
+ * it keeps the previous call's contents; each launch writes every partial it
+ * later reads, so nothing has to be cleared between calls.  Calls whose
+ * execution overlaps on the GPU (different streams, or several host threads)
+ * race on the array: serialise them.
+ */
+#define SS_DECODE_STATIC_SCRATCH_BYTES (16u << 20)
+ss_status ss_attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                 void* o, int B, int Hq, int Hkv, int Lk, int d, float scale,
+                                 float lambda, int num_kv_splits, uint32_t* skip_counts,
+                                 void* stream);
+
 /* A calibration problem: the inputs the threshold is fitted on. */
 typedef enum { SS_PREFILL = 0, SS_DECODE = 1 } ss_kind;
 typedef struct {

@@ -1,0 +1,82 @@
+"""ss_attn_decode_noalloc: decode for callers that cannot allocate device memory.
+
+Some callers are handed only their input and output buffers -- a plugin
+inside an inference engine that owns all device memory, or a serving loop
+that must not call cudaMalloc mid-flight -- so they cannot pass
+ss_attn_decode's workspace.  This entry point keeps the split partials in a
+fixed device array inside the library instead.  The test calls it through the
+C ABI twice in a row (different inputs and lambda, so stale contents from the
+first call would show up in the second) and compares each result with the
+regular workspace entry point's, within the tolerance the parity tests use.
+It also checks that a problem too large for the built-in array is refused.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS, MEAN_ABS = 2e-2, 2e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import block_sparse_attention_sm_gb300 as ss
+
+    ss.build()
+    assert torch.cuda.is_available()
+
+
+def _inputs(B, Hq, Hkv, Lk, d, seed):
+    from block_sparse_attention_sm_gb300 import synth
+
+    return synth.decode_inputs(B=B, Hq=Hq, Hkv=Hkv, Lk=Lk, d=d, hot_frac=0.15, seed=seed,
+                               device="cuda")
+
+
+def _with_workspace(capi, inp, lam, S):
+    B, Hq, d = inp.q.shape
+    Hkv, Lk = inp.k.shape[1], inp.k.shape[2]
+    n = capi.ss_attn_decode_workspace_size(B, Hq, d, S)
+    ws = torch.empty(max(n, 16), dtype=torch.uint8, device="cuda")
+    o = torch.empty_like(inp.q)
+    counts = torch.full((B * Hkv * S,), -1, dtype=torch.int32, device="cuda")
+    st = capi.ss_attn_decode(inp.q, inp.k, inp.v, o, B, Hq, Hkv, Lk, d, 1.0 / math.sqrt(d), lam,
+                             S, counts, ws, n)
+    assert st == capi.SS_OK, capi.ss_status_string(st)
+    return o, counts
+
+
+def test_noalloc_decode_matches_workspace_entry_point_twice():
+    from block_sparse_attention_sm_gb300 import capi
+
+    cases = [  # (B, Hq, Hkv, Lk, d, splits, seed, a)
+        (8, 32, 8, 4096, 128, 8, 0, 4.0),
+        (4, 8, 2, 3000, 64, 5, 1, 1.5),
+    ]
+    for B, Hq, Hkv, Lk, d, S, seed, a in cases:
+        inp = _inputs(B, Hq, Hkv, Lk, d, seed)
+        lam = a / Lk
+        ref_o, ref_counts = _with_workspace(capi, inp, lam, S)
+        o = torch.full_like(inp.q, float("nan"))
+        counts = torch.full((B * Hkv * S,), -1, dtype=torch.int32, device="cuda")
+        st = capi.ss_attn_decode_noalloc(inp.q, inp.k, inp.v, o, B, Hq, Hkv, Lk, d,
+                                         1.0 / math.sqrt(d), lam, S, counts)
+        assert st == capi.SS_OK, capi.ss_status_string(st)
+        assert capi.ss_stream_status() == capi.SS_OK
+        err = (o.float() - ref_o.float()).abs()
+        assert float(err.max()) <= MAX_ABS and float(err.mean()) <= MEAN_ABS
+        assert torch.equal(counts, ref_counts)
+        assert int(counts.sum()) > 0  # the sparse path was exercised
+
+
+def test_noalloc_rejects_problems_beyond_the_static_array():
+    from block_sparse_attention_sm_gb300 import capi
+
+    B, Hq, d, S = 64, 32, 128, 16  # 64*32*16*130*4 bytes = 17 MB > 16 MiB
+    assert capi.ss_attn_decode_workspace_size(B, Hq, d, S) > capi.SS_DECODE_STATIC_SCRATCH_BYTES
+    q = torch.empty(16, dtype=torch.bfloat16, device="cuda")  # never read: refused first
+    st = capi.ss_attn_decode_noalloc(q, q, q, q, B, Hq, 8, 32768, d, 0.1, 0.01, S, None)
+    assert st == capi.SS_ERR_WORKSPACE
