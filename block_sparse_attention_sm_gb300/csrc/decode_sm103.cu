@@ -8,12 +8,12 @@
 // decisions are taken a chunk of tiles at a time and the surviving V tiles of
 // that chunk are fetched as one batch, while the next chunk's scores run.
 //
-// One CTA = one (sequence b, KV head, split); 256 threads (8 warps).  The G
+// One CTA = one (sequence b, KV head, split); 512 threads (256 for 8-row groups).  The G
 // query heads sharing the KV head (one token each) form the voting group:
 // a tile is skipped only if every one of them passes the test.
 //
 // Pipeline per chunk c of 2 tiles (iteration c):
-//   A(c)   scores of tiles 2c, 2c+1 (warps 0-3 / 4-7, 32 keys per warp) from
+//   A(c)   scores of tiles 2c, 2c+1 (each by half of the warps) from
 //          the K ring (4 stages, 1-D bulk copies of contiguous 128-key tiles);
 //          then the two freed K stages are refilled 2 chunks ahead.
 //   C(c-1) online softmax + P.V over the survivors of chunk c-1 (their V
@@ -32,17 +32,21 @@ namespace ssattn {
 
 namespace {
 
-constexpr int kDecThreads = 256;
 constexpr int kKStages = 4;
 
 template <int D, int GP>
 struct DecodeCfg {
+  // 16 warps (8 per tile of a chunk) hide shared-memory latency; the
+  // 8-row vote group keeps 8 warps to stay within the register budget.
+  static constexpr int kThreads = (GP >= 8) ? 256 : 512;
+  static constexpr int kWarpsPerTile = kThreads / 64;
+  static constexpr int kKeysPerWarp = kTile / kWarpsPerTile;
   static constexpr int kTileBytes = kTile * D * 2;
   static constexpr int kLPR = D / 8;           // lanes per key row (16-byte slices)
   static constexpr int kKPI = 32 / kLPR;       // keys per warp iteration
-  static constexpr int kIters = 32 / kKPI;     // iterations for the warp's 32 keys
+  static constexpr int kIters = kKeysPerWarp / kKPI;  // iterations for the warp's keys
   static constexpr int kNDP = D / 2;           // threads per key group in P.V (bf16 pairs)
-  static constexpr int kNKG = kDecThreads / kNDP;  // key groups
+  static constexpr int kNKG = kThreads / kNDP;  // key groups
   static constexpr int kKPG = kTile / kNKG;    // keys per group
   // shared memory layout (bytes, 16-byte aligned pieces)
   static constexpr int kKOff = 0;
@@ -77,8 +81,9 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& raw, float (&f)[8]) {
 }
 
 template <int D, int GP, Mode MODE>
-__global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(DecodeCfg<D, GP>::kThreads, 1) decode_kernel(const DecodeParams p) {
   using C = DecodeCfg<D, GP>;
+  constexpr int kDecThreads = C::kThreads;
   constexpr bool kPV = (MODE != Mode::kCount);
   constexpr bool kVote = (MODE != Mode::kDense);
   extern __shared__ __align__(128) uint8_t smem[];
@@ -160,7 +165,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecodePara
     const int cb = c & 1;
     // ---------------------------------------------------------------- A(c)
     if (c < nchunks) {
-      const int tl = warp >> 2;
+      const int tl = warp / C::kWarpsPerTile;
       const int t = 2 * c + tl;
       if (t < nt) {
         const int st = t % kKStages;
@@ -170,7 +175,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecodePara
           float* sc = SC(cb, tl, 0);
 #pragma unroll 4
           for (int it = 0; it < C::kIters; ++it) {
-            const int key = (warp & 3) * 32 + it * C::kKPI + lane / C::kLPR;
+            const int key = (warp % C::kWarpsPerTile) * C::kKeysPerWarp + it * C::kKPI + lane / C::kLPR;
             const uint4 raw =
                 *reinterpret_cast<const uint4*>(kt + key * D * 2 + (lane % C::kLPR) * 16);
             float kf[8];
@@ -441,7 +446,7 @@ cudaError_t launch_dec(const DecodeParams& p, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const long ctas = static_cast<long>(p.B) * p.Hkv * p.S;
-  fn<<<dim3(static_cast<unsigned>(ctas)), dim3(kDecThreads), C::kSmemBytes, st>>>(p);
+  fn<<<dim3(static_cast<unsigned>(ctas)), dim3(C::kThreads), C::kSmemBytes, st>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess || MODE == Mode::kCount || p.S == 1) return e;
   const int rows = p.B * p.Hq;
