@@ -11,9 +11,8 @@
 // K/V tile; 384 threads (3 warpgroups; registers re-split with setmaxnreg):
 //   warps 0-3 / 4-7  softmax of query block 0 / 1: thread = query row = TMEM
 //                    lane.  It loads its 128 scores from TMEM once, takes the
-//                    row maximum, votes (per-warp __all_sync, combined over the
-//                    block's four warps through shared memory and an
-//                    mbarrier) and, for kept tiles, writes P as bf16 over the
+//                    row maximum, votes (a bar.red.and over the block's 128
+//                    threads) and, for kept tiles, writes P as bf16 over the
 //                    first 64 columns of S; lazy O rescale; epilogue O / l.
 //   warp 8           TMA producer: both Q blocks, then the K ring.
 //   warp 9           TMA producer: the V ring.
@@ -73,13 +72,11 @@ struct PrefillCtl {
   uint64_t k_full[NK], k_empty[NK];
   uint64_t v_full[NV], v_empty[NV];
   uint64_t s_full[2], p_full[2];
-  uint64_t vote_bar[2][2];  // [block][tile parity], one arrival per softmax warp
   uint64_t o_done;
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort_flag;
   int dec[2];
-  int verdict[2][2][4];
   float red[2][2][4];
 };
 
@@ -140,8 +137,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = 0; t < 2; ++t) {
       mbar_init(&ctl->s_full[t], 1);
       mbar_init(&ctl->p_full[t], 128);
-      mbar_init(&ctl->vote_bar[t][0], 4);
-      mbar_init(&ctl->vote_bar[t][1], 4);
     }
     mbar_init(&ctl->o_done, 1);
     mbar_init(&ctl->mma_done, 1);
@@ -355,8 +350,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
     };
 
+    // Vote path: the block's four warps meet at named barrier 2 + t once per
+    // tile (bar.red), and no thread may skip it -- a failed wait is carried
+    // to the barrier and the warps leave the loop together.  The dense path
+    // has no barrier inside the loop and leaves on its own.
+    const bool team = kVote || p.margin != nullptr;
+    const uint32_t bar_id = 2 + t;
     for (int i = 0; i < n_mine; ++i) {
-      if (!wwait(&ctl->s_full[t], i & 1)) {
+      const bool got = wwait(&ctl->s_full[t], i & 1);
+      if (!got && !team) {
         ok = false;
         break;
       }
@@ -369,9 +371,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // All 128 scores of the row in registers (one TMEM round trip); masked
       // keys become -inf; four independent partial maxima.
       uint32_t sr[128];
+      if (got) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32p(colS + 32 * c, sr + 32 * c);
-      tmem_wait_ld();
+        for (int c = 0; c < 4; ++c) tmem_ld32p(colS + 32 * c, sr + 32 * c);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int e = 0; e < 128; ++e) sr[e] = __float_as_uint(-INFINITY);
+      }
       float mx[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) mx[e] = -INFINITY;
@@ -390,31 +397,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Skip vote: every row of the block must pass exp(scale*(tmax - m)) < lambda.
       // (The dense path runs the same reduction only to report margins.)
       bool skip = false;
-      if (kVote || p.margin != nullptr) {
+      if (team) {
         float c_r = -INFINITY;  // a row with no visible key does not veto
         if (tmax != -INFINITY) c_r = (m_true == -INFINITY) ? INFINITY : tmax - m_true;
-        const bool warp_pass = __all_sync(0xffffffffu, c_r < p.thr_raw);
-        float cm = c_r;
-        if (p.margin != nullptr) {
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
-        }
-        const int vb = i & 1;
-        if (lane == 0) {
-          *reinterpret_cast<volatile int*>(&ctl->verdict[t][vb][warp & 3]) = warp_pass ? 1 : 0;
-          *reinterpret_cast<volatile float*>(&ctl->red[t][vb][warp & 3]) = cm;
-          mbar_arrive(&ctl->vote_bar[t][vb]);
-        }
-        if (!wwait(&ctl->vote_bar[t][vb], (i >> 1) & 1)) {
+        const bool all_pass = named_bar_and(bar_id, 128, got && c_r < p.thr_raw);
+        if (!all_pass && named_bar_or(bar_id, 128, !got)) {
           ok = false;
           break;
         }
-        const volatile int* vv = ctl->verdict[t][vb];
-        skip = kVote && vv[0] && vv[1] && vv[2] && vv[3];
-        if (tid_t == 0 && p.margin != nullptr) {
-          const volatile float* rr = ctl->red[t][vb];
-          const float cmax = fmaxf(fmaxf(rr[0], rr[1]), fmaxf(rr[2], rr[3]));
-          p.margin[unit * p.nT + i] = (cmax == INFINITY) ? INFINITY : cmax * p.scale;
+        skip = kVote && all_pass;
+        if (p.margin != nullptr) {
+          float cm = c_r;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
+          if (lane == 0) *reinterpret_cast<volatile float*>(&ctl->red[t][i & 1][warp & 3]) = cm;
+          named_bar_sync(bar_id, 128);
+          if (tid_t == 0) {
+            const volatile float* rr = ctl->red[t][i & 1];
+            const float cmax = fmaxf(fmaxf(rr[0], rr[1]), fmaxf(rr[2], rr[3]));
+            p.margin[unit * p.nT + i] = (cmax == INFINITY) ? INFINITY : cmax * p.scale;
+          }
         }
       }
       m_true = fmaxf(m_true, tmax);
