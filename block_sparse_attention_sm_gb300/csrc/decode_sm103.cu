@@ -42,7 +42,7 @@ struct DecodeCfg {
   static constexpr int kWarpsPerTile = kThreads / 64;
   static constexpr int kKeysPerWarp = kTile / kWarpsPerTile;
   static constexpr int kTileBytes = kTile * D * 2;
-  static constexpr int kLPR = D / 8;           // lanes per key row (16-byte slices)
+  static constexpr int kLPR = D / 16;          // lanes per key row (two 16-byte chunks each)
   static constexpr int kKPI = 32 / kLPR;       // keys per warp iteration
   static constexpr int kIters = kKeysPerWarp / kKPI;  // iterations for the warp's keys
   static constexpr int kNDP = D / 2;           // threads per key group in P.V (bf16 pairs)
@@ -70,6 +70,23 @@ struct DecodeCtl {
   int surv_tile[2];
   uint32_t surv_par[2];
 };
+
+// Packed fp32 pair arithmetic (two IEEE fp32 FMAs per instruction).
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+  return static_cast<uint64_t>(__float_as_uint(lo)) | (static_cast<uint64_t>(__float_as_uint(hi)) << 32);
+}
+// bf16 pair (one 32-bit word) -> fp32 pair (exact: bf16 is the upper half).
+__device__ __forceinline__ uint64_t bf16x2_to_f32x2(uint32_t w) {
+  return static_cast<uint64_t>(w << 16) | (static_cast<uint64_t>(w & 0xffff0000u) << 32);
+}
+__device__ __forceinline__ float f32x2_sum(uint64_t v) {
+  return __uint_as_float(static_cast<uint32_t>(v)) + __uint_as_float(static_cast<uint32_t>(v >> 32));
+}
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& raw, float (&f)[8]) {
   const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
@@ -139,14 +156,18 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::kThreads, 1) decode_kernel(c
   if (tid == 0)
     for (int t = 0; t < min(nt, kKStages); ++t) issue_k(t);
 
-  // Per-lane query slice for the score phase.
-  float qv[GP][8];
+  // Per-lane query slice for the score phase: the lane owns 16 dimensions,
+  // chunks c and c + kLPR of eight (c = lane % kLPR), as fp32 pairs.
+  uint64_t qp[GP][8];
   {
-    const int e0 = (lane % C::kLPR) * 8;
+    const int e0 = (lane % C::kLPR) * 8, e1 = e0 + C::kLPR * 8;
 #pragma unroll
     for (int g = 0; g < GP; ++g)
 #pragma unroll
-      for (int e = 0; e < 8; ++e) qv[g][e] = sQ[g * D + e0 + e];
+      for (int j = 0; j < 4; ++j) {
+        qp[g][j] = pack_f32x2(sQ[g * D + e0 + 2 * j], sQ[g * D + e0 + 2 * j + 1]);
+        qp[g][4 + j] = pack_f32x2(sQ[g * D + e1 + 2 * j], sQ[g * D + e1 + 2 * j + 1]);
+      }
   }
 
   // Running state.  Thread 0: exact running max per row for the vote.
@@ -173,20 +194,30 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::kThreads, 1) decode_kernel(c
           const uint8_t* kt = sK + st * C::kTileBytes;
           const int valid = tile_rows(t);
           float* sc = SC(cb, tl, 0);
-#pragma unroll 4
+#pragma unroll 2
           for (int it = 0; it < C::kIters; ++it) {
             const int key = (warp % C::kWarpsPerTile) * C::kKeysPerWarp + it * C::kKPI + lane / C::kLPR;
-            const uint4 raw =
-                *reinterpret_cast<const uint4*>(kt + key * D * 2 + (lane % C::kLPR) * 16);
-            float kf[8];
-            bf16x8_to_f32(raw, kf);
+            // Two 16-byte chunks of the key row.  For d = 128 the first load
+            // of the warp covers bytes [0,128) of its four rows (all eight
+            // bank groups); for d = 64 the chunk order alternates with the
+            // key's parity for the same reason.
+            const int c = lane % C::kLPR;
+            const bool swap = (D == 64) && (key & 1);
+            const uint8_t* row = kt + key * D * 2;
+            const uint4 r0 = *reinterpret_cast<const uint4*>(row + (swap ? c + C::kLPR : c) * 16);
+            const uint4 r1 = *reinterpret_cast<const uint4*>(row + (swap ? c : c + C::kLPR) * 16);
+            const uint4 ra = swap ? r1 : r0, rb = swap ? r0 : r1;
+            const uint32_t w[8] = {ra.x, ra.y, ra.z, ra.w, rb.x, rb.y, rb.z, rb.w};
+            uint64_t kp[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) kp[j] = bf16x2_to_f32x2(w[j]);
             float part[GP];
 #pragma unroll
             for (int g = 0; g < GP; ++g) {
-              float a = 0.f;
+              uint64_t a = 0;
 #pragma unroll
-              for (int e = 0; e < 8; ++e) a = fmaf(qv[g][e], kf[e], a);
-              part[g] = a;
+              for (int j = 0; j < 8; ++j) a = ffma2(qp[g][j], kp[j], a);
+              part[g] = f32x2_sum(a);
             }
             // Transpose-reduce over the kLPR lanes of this key: each halving
             // step hands half of the rows to the partner lane, so the lane
@@ -214,7 +245,13 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::kThreads, 1) decode_kernel(c
                 writer = writer && !upper;
               }
             }
-            if (writer && gsel < G) sc[gsel * kTile + key] = (key < valid) ? part[0] : -INFINITY;
+            // The lane now holds the complete dot products of rows
+            // gsel .. gsel + n - 1 (n > 1 only when the lanes of a key are
+            // fewer than the rows of the group).
+#pragma unroll
+            for (int j = 0; j < GP; ++j)
+              if (j < n && writer && gsel + j < G)
+                sc[(gsel + j) * kTile + key] = (key < valid) ? part[j] : -INFINITY;
           }
         }
       }

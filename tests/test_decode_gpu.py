@@ -28,6 +28,7 @@ SHAPES = [
     (2, 6, 2, 1500, 64, 4),     # G = 3 (padded vote group)
     (1, 4, 1, 100, 128, 1),     # one partial tile
     (1, 4, 1, 300, 128, 8),     # more splits than tiles: empty splits
+    (2, 8, 1, 900, 64, 3),      # d = 64 with an 8-row vote group
 ]
 
 
