@@ -12,15 +12,15 @@
 // query heads sharing the KV head (one token each) form the voting group:
 // a tile is skipped only if every one of them passes the test.
 //
-// Pipeline per chunk c of 2 tiles (iteration c):
-//   A(c)   scores of tiles 2c, 2c+1 (each by half of the warps) from
-//          the K ring (4 stages, 1-D bulk copies of contiguous 128-key tiles);
-//          then the two freed K stages are refilled 2 chunks ahead.
-//   C(c-1) online softmax + P.V over the survivors of chunk c-1 (their V
-//          tiles were issued at the end of the previous iteration).
-//   B(c)   per-row tile maxima, the vote (exact running maximum, one thread),
-//          counters / mask / margin, and the batch of V loads for chunk c's
-//          survivors.
+// Pipeline per chunk c of 2 tiles (iteration c), two block barriers:
+//   A(c)    scores of tiles 2c, 2c+1 (each by half of the warps) from the K
+//           ring (4 stages, 1-D bulk copies of contiguous 128-key tiles),
+//           plus per-warp partial row maxima;
+//   -- barrier; the two freed K stages are refilled 2 chunks ahead;
+//   vote(c) one warp (lane = row): tile maxima, the vote with the exact
+//           running maximum, counters / mask / margin, survivor list;
+//   C(c-1)  meanwhile, online softmax + P.V over chunk c-1's survivors;
+//   -- barrier; the batch of V loads for chunk c's survivors is issued.
 // Scores use fp32 FMAs on bf16 K read from shared memory (the contraction
 // has only G <= 8 rows; the kernel is bound by the K stream, not by math).
 #include <cuda_bf16.h>
@@ -33,6 +33,15 @@ namespace ssattn {
 namespace {
 
 constexpr int kKStages = 4;
+
+struct DecodeCtl {
+  uint64_t k_full[kKStages];
+  uint64_t v_full[2];
+  int abort_flag;
+  int n_surv[2];           // [chunk parity]
+  int surv_tile[2][2];     // [chunk parity][slot]
+  uint32_t surv_par[2][2];
+};
 
 template <int D, int GP>
 struct DecodeCfg {
@@ -57,19 +66,14 @@ struct DecodeCfg {
   static constexpr int kTmOff = kPOff + 2 * kTile * GP * 4;            // float [2][2][GP]
   static constexpr int kAlOff = kTmOff + 2 * 2 * GP * 4;               // float [2][GP]
   static constexpr int kMlOff = kAlOff + 2 * GP * 4;                   // float [GP][2]
-  static constexpr int kCtlOff = (kMlOff + GP * 2 * 4 + 15) / 16 * 16;
+  static constexpr int kPmOff = kMlOff + GP * 2 * 4;                   // float [2][2][WPT][GP]
+  static constexpr int kCtlOff = (kPmOff + 2 * 2 * kWarpsPerTile * GP * 4 + 15) / 16 * 16;
+  static constexpr int kVoteWarp = kThreads / 32 - 1;
   static constexpr int kSmemBytes = kCtlOff + 128;
+  static_assert(sizeof(DecodeCtl) <= 128, "control block overflow");
   static_assert(kNKG * GP * D * 4 <= kKStages * kTileBytes, "reduction buffer must fit the K ring");
 };
 
-struct DecodeCtl {
-  uint64_t k_full[kKStages];
-  uint64_t v_full[2];
-  int abort_flag;
-  int n_surv;
-  int surv_tile[2];
-  uint32_t surv_par[2];
-};
 
 // Packed fp32 pair arithmetic (two IEEE fp32 FMAs per instruction).
 __device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
@@ -112,6 +116,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::kThreads, 1) decode_kernel(c
   float* sTm = reinterpret_cast<float*>(smem + C::kTmOff);
   float* sAl = reinterpret_cast<float*>(smem + C::kAlOff);
   float* sMl = reinterpret_cast<float*>(smem + C::kMlOff);
+  float* sPm = reinterpret_cast<float*>(smem + C::kPmOff);
   auto* ctl = reinterpret_cast<DecodeCtl*>(smem + C::kCtlOff);
   volatile int* abort_flag = &ctl->abort_flag;
   auto SC = [&](int buf, int tl, int g) { return sSc + ((buf * 2 + tl) * GP + g) * kTile; };
@@ -132,7 +137,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::kThreads, 1) decode_kernel(c
     for (int s = 0; s < kKStages; ++s) mbar_init(&ctl->k_full[s], 1);
     for (int s = 0; s < 2; ++s) mbar_init(&ctl->v_full[s], 1);
     ctl->abort_flag = 0;
-    ctl->n_surv = 0;
+    ctl->n_surv[0] = ctl->n_surv[1] = 0;
     fence_mbar_init();
   }
   // Query rows of the group (fp32 copy; padding rows are zero).
@@ -170,11 +175,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::kThreads, 1) decode_kernel(c
       }
   }
 
-  // Running state.  Thread 0: exact running max per row for the vote.
+  // Running state.  Vote warp, lane g: exact running max of row g.
   // Warp g (< GP): softmax state of row g (all lanes hold the same values).
-  float mt[GP];
-#pragma unroll
-  for (int g = 0; g < GP; ++g) mt[g] = -INFINITY;
+  float mt = -INFINITY;
   float m_run = -INFINITY, l_run = 0.f;
   float acc[GP][2];
 #pragma unroll
@@ -185,15 +188,23 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::kThreads, 1) decode_kernel(c
   for (int c = 0; c <= nchunks; ++c) {
     const int cb = c & 1;
     // ---------------------------------------------------------------- A(c)
+    // Scores of tiles 2c, 2c+1 (half of the warps each), plus each warp's
+    // partial row maxima for the vote.
     if (c < nchunks) {
       const int tl = warp / C::kWarpsPerTile;
       const int t = 2 * c + tl;
       if (t < nt) {
         const int st = t % kKStages;
-        if (mbar_wait(&ctl->k_full[st], (t / kKStages) & 1, abort_flag)) {
+        // warp-uniform: the loop below shuffles across the whole warp
+        if (__all_sync(0xffffffffu, mbar_wait(&ctl->k_full[st], (t / kKStages) & 1, abort_flag))) {
           const uint8_t* kt = sK + st * C::kTileBytes;
           const int valid = tile_rows(t);
           float* sc = SC(cb, tl, 0);
+          float rmax[GP];
+#pragma unroll
+          for (int j = 0; j < GP; ++j) rmax[j] = -INFINITY;
+          int gsel = 0, n = GP;
+          bool writer = true;
 #pragma unroll 2
           for (int it = 0; it < C::kIters; ++it) {
             const int key = (warp % C::kWarpsPerTile) * C::kKeysPerWarp + it * C::kKPI + lane / C::kLPR;
@@ -201,11 +212,11 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::kThreads, 1) decode_kernel(c
             // of the warp covers bytes [0,128) of its four rows (all eight
             // bank groups); for d = 64 the chunk order alternates with the
             // key's parity for the same reason.
-            const int c = lane % C::kLPR;
+            const int cc = lane % C::kLPR;
             const bool swap = (D == 64) && (key & 1);
             const uint8_t* row = kt + key * D * 2;
-            const uint4 r0 = *reinterpret_cast<const uint4*>(row + (swap ? c + C::kLPR : c) * 16);
-            const uint4 r1 = *reinterpret_cast<const uint4*>(row + (swap ? c : c + C::kLPR) * 16);
+            const uint4 r0 = *reinterpret_cast<const uint4*>(row + (swap ? cc + C::kLPR : cc) * 16);
+            const uint4 r1 = *reinterpret_cast<const uint4*>(row + (swap ? cc : cc + C::kLPR) * 16);
             const uint4 ra = swap ? r1 : r0, rb = swap ? r0 : r1;
             const uint32_t w[8] = {ra.x, ra.y, ra.z, ra.w, rb.x, rb.y, rb.z, rb.w};
             uint64_t kp[8];
@@ -221,10 +232,11 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::kThreads, 1) decode_kernel(c
             }
             // Transpose-reduce over the kLPR lanes of this key: each halving
             // step hands half of the rows to the partner lane, so the lane
-            // ends up holding the full dot product of row `gsel`.
-            int gsel = 0;
-            bool writer = true;
-            int n = GP;
+            // ends up holding the full dot products of rows gsel .. gsel+n-1
+            // (n > 1 only when a key has fewer lanes than the group rows).
+            gsel = 0;
+            n = GP;
+            writer = true;
 #pragma unroll
             for (int o = C::kLPR / 2; o >= 1; o >>= 1) {
               const bool upper = (lane & o) != 0;
@@ -245,13 +257,25 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::kThreads, 1) decode_kernel(c
                 writer = writer && !upper;
               }
             }
-            // The lane now holds the complete dot products of rows
-            // gsel .. gsel + n - 1 (n > 1 only when the lanes of a key are
-            // fewer than the rows of the group).
 #pragma unroll
-            for (int j = 0; j < GP; ++j)
-              if (j < n && writer && gsel + j < G)
-                sc[(gsel + j) * kTile + key] = (key < valid) ? part[j] : -INFINITY;
+            for (int j = 0; j < GP; ++j) {
+              if (j < n) {
+                const float sv = (key < valid) ? part[j] : -INFINITY;
+                rmax[j] = fmaxf(rmax[j], sv);
+                if (writer && gsel + j < G) sc[(gsel + j) * kTile + key] = sv;
+              }
+            }
+          }
+          // Partial maxima of this warp's keys: combine over the lanes that
+          // hold the same rows for different keys.
+#pragma unroll
+          for (int j = 0; j < GP; ++j) {
+            if (j < n) {
+#pragma unroll
+              for (int o = C::kLPR; o < 32; o <<= 1) rmax[j] = fmaxf(rmax[j], __shfl_xor_sync(0xffffffffu, rmax[j], o));
+              if (lane < C::kLPR && writer && gsel + j < G)
+                sPm[((cb * 2 + tl) * C::kWarpsPerTile + warp % C::kWarpsPerTile) * GP + gsel + j] = rmax[j];
+            }
           }
         }
       }
@@ -262,18 +286,55 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::kThreads, 1) decode_kernel(c
       for (int t = 2 * c + kKStages; t < min(nt, 2 * c + kKStages + 2); ++t) issue_k(t);
     }
 
+    // ---------------------------------------------------------------- vote(c)
+    // One warp, lane g = row g: tile maxima from the partials, the vote with
+    // the exact running maximum, counters and the survivor list of chunk c.
+    if (c < nchunks && warp == C::kVoteWarp) {
+      int ns = 0;
+      for (int tl = 0; tl < 2; ++tl) {
+        const int t = 2 * c + tl;
+        if (t >= nt) break;
+        float tm = -INFINITY;
+        if (lane < G)
+#pragma unroll
+          for (int w2 = 0; w2 < C::kWarpsPerTile; ++w2)
+            tm = fmaxf(tm, sPm[((cb * 2 + tl) * C::kWarpsPerTile + w2) * GP + lane]);
+        float cval = -INFINITY;
+        if (lane < G && tm != -INFINITY) cval = (mt == -INFINITY) ? INFINITY : tm - mt;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) cval = fmaxf(cval, __shfl_xor_sync(0xffffffffu, cval, o));
+        const bool skip = kVote && (cval < p.thr_raw);
+        if (lane < G) {
+          mt = fmaxf(mt, tm);
+          sTm[(cb * 2 + tl) * GP + lane] = tm;
+        }
+        if (lane == 0) {
+          const long gi = static_cast<long>(bk) * p.nT + j0 + t;
+          if (p.mask != nullptr) p.mask[gi] = skip ? 1 : 0;
+          if (p.margin != nullptr) p.margin[gi] = (cval == INFINITY) ? INFINITY : cval * p.scale;
+          if (skip) ++skipped;
+          else if (kPV) ctl->surv_tile[cb][ns] = t;
+        }
+        if (!skip && kPV) ++ns;
+      }
+      if (lane == 0) ctl->n_surv[cb] = ns;
+    }
+
     // ---------------------------------------------------------------- C(c-1)
+    // Online softmax + P.V over the survivors of chunk c-1 (their V tiles
+    // were fetched after the previous iteration's barrier).
     if (kPV && c >= 1) {
       const int pc = c - 1, pcb = pc & 1;
-      const int ns = ctl->n_surv;
+      const int ns = ctl->n_surv[pcb];
       if (ns > 0) {
         bool ok = true;
-        for (int s = 0; s < ns; ++s) ok = ok && mbar_wait(&ctl->v_full[s], ctl->surv_par[s], abort_flag);
+        for (int s2 = 0; s2 < ns; ++s2)
+          ok = ok && mbar_wait(&ctl->v_full[s2], ctl->surv_par[pcb][s2], abort_flag);
         if (warp < GP) {
           const int g = warp;
-          for (int s = 0; s < ns; ++s) {
-            const int tl = ctl->surv_tile[s] - 2 * pc;
-            float* prow = sP + s * kTile * GP;
+          for (int s2 = 0; s2 < ns; ++s2) {
+            const int tl = ctl->surv_tile[pcb][s2] - 2 * pc;
+            float* prow = sP + s2 * kTile * GP;
             if (g < G) {
               const float tm = sTm[(pcb * 2 + tl) * GP + g];
               const float m_new = fmaxf(m_run, tm);
@@ -292,34 +353,34 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::kThreads, 1) decode_kernel(c
               for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
               l_run = alpha * l_run + sum;
               m_run = m_new;
-              if (lane == 0) sAl[s * GP + g] = alpha;
+              if (lane == 0) sAl[s2 * GP + g] = alpha;
             } else {
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk) prow[(lane + 32 * kk) * GP + g] = 0.f;
-              if (lane == 0) sAl[s * GP + g] = 1.f;
+              if (lane == 0) sAl[s2 * GP + g] = 1.f;
             }
           }
         }
         __syncthreads();
         if (ok) {
           const int dp = tid % C::kNDP, kg = tid / C::kNDP;
-          for (int s = 0; s < ns; ++s) {
+          for (int s2 = 0; s2 < ns; ++s2) {
 #pragma unroll
             for (int g = 0; g < GP; ++g) {
-              const float a = sAl[s * GP + g];
+              const float a = sAl[s2 * GP + g];
               acc[g][0] *= a;
               acc[g][1] *= a;
             }
-            const int valid = tile_rows(ctl->surv_tile[s]);
-            const uint8_t* vt = sV + s * C::kTileBytes;
-            const float* prow = sP + s * kTile * GP;
+            const int valid = tile_rows(ctl->surv_tile[pcb][s2]);
+            const uint8_t* vt = sV + s2 * C::kTileBytes;
+            const float* prow = sP + s2 * kTile * GP;
             const int k0 = kg * C::kKPG;
             const int kend = min(C::kKPG, valid - k0);
 #pragma unroll 4
             for (int kk = 0; kk < kend; ++kk) {
               const int k = k0 + kk;
-              const uint32_t w = *reinterpret_cast<const uint32_t*>(vt + k * D * 2 + dp * 4);
-              const float v0 = __uint_as_float(w << 16), v1 = __uint_as_float(w & 0xffff0000u);
+              const uint32_t wv = *reinterpret_cast<const uint32_t*>(vt + k * D * 2 + dp * 4);
+              const float v0 = __uint_as_float(wv << 16), v1 = __uint_as_float(wv & 0xffff0000u);
               float pk[GP];
               if constexpr (GP >= 4) {
 #pragma unroll
@@ -341,57 +402,22 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::kThreads, 1) decode_kernel(c
         }
       }
     }
-
-    // ---------------------------------------------------------------- B(c)
-    if (c < nchunks) {
-      for (int q = warp; q < 2 * G; q += kDecThreads / 32) {
-        const int tl = q / G, g = q - (q / G) * G;
-        if (2 * c + tl < nt) {
-          const float* sc = SC(cb, tl, g);
-          float m = fmaxf(fmaxf(sc[lane], sc[lane + 32]), fmaxf(sc[lane + 64], sc[lane + 96]));
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-          if (lane == 0) sTm[(cb * 2 + tl) * GP + g] = m;
-        }
-      }
-      __syncthreads();
-      if (tid == 0) {
-        int ns = 0;
-        for (int tl = 0; tl < 2 && 2 * c + tl < nt; ++tl) {
-          const int t = 2 * c + tl;
-          float cval = -INFINITY;
-#pragma unroll
-          for (int g = 0; g < GP; ++g) {
-            if (g < G) {
-              const float tm = sTm[(cb * 2 + tl) * GP + g];
-              if (tm != -INFINITY) cval = fmaxf(cval, (mt[g] == -INFINITY) ? INFINITY : tm - mt[g]);
-              mt[g] = fmaxf(mt[g], tm);
-            }
-          }
-          const bool skip = kVote && (cval < p.thr_raw);
-          const long gi = static_cast<long>(bk) * p.nT + j0 + t;
-          if (p.mask != nullptr) p.mask[gi] = skip ? 1 : 0;
-          if (p.margin != nullptr) p.margin[gi] = (cval == INFINITY) ? INFINITY : cval * p.scale;
-          if (skip) {
-            ++skipped;
-          } else if (kPV) {
-            // Batched V fetch of this chunk's survivors (§Kernel-ontwerp).
-            const uint32_t bytes = static_cast<uint32_t>(tile_rows(t)) * D * 2;
-            ctl->surv_tile[ns] = t;
-            ctl->surv_par[ns] = nv_issued[ns] & 1u;
-            if (!*abort_flag) {
-              mbar_arrive_expect_tx(&ctl->v_full[ns], bytes);
-              bulk_load(sV + ns * C::kTileBytes, vbase + static_cast<size_t>(j0 + t) * kTile * D,
-                        bytes, &ctl->v_full[ns]);
-              ++nv_issued[ns];
-            }
-            ++ns;
-          }
-        }
-        ctl->n_surv = ns;
+    __syncthreads();
+    // ---------------------------------------------------------------- V(c)
+    // Batched fetch of chunk c's surviving V tiles (BLASST §Kernel-ontwerp):
+    // the slots are free now that C(c-1) is done.
+    if (kPV && tid == 0 && c < nchunks && !*abort_flag) {
+      const int ns = ctl->n_surv[cb];
+      for (int s2 = 0; s2 < ns; ++s2) {
+        const int t = ctl->surv_tile[cb][s2];
+        const uint32_t bytes = static_cast<uint32_t>(tile_rows(t)) * D * 2;
+        ctl->surv_par[cb][s2] = nv_issued[s2] & 1u;
+        mbar_arrive_expect_tx(&ctl->v_full[s2], bytes);
+        bulk_load(sV + s2 * C::kTileBytes, vbase + static_cast<size_t>(j0 + t) * kTile * D, bytes,
+                  &ctl->v_full[s2]);
+        ++nv_issued[s2];
       }
     }
-    __syncthreads();
   }
 
   // ------------------------------------------------------------------ output
@@ -428,8 +454,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::kThreads, 1) decode_kernel(c
       }
     }
   }
+  if (warp == C::kVoteWarp && lane == 0 && p.counts != nullptr)
+    p.counts[static_cast<long>(bk) * p.S + split] = skipped;
   if (tid == 0) {
-    if (p.counts != nullptr) p.counts[static_cast<long>(bk) * p.S + split] = skipped;
     if (*abort_flag) {
       // Let in-flight copies land before shared memory is released.
       for (int s = 0; s < kKStages; ++s)
