@@ -32,7 +32,7 @@ class SSError(RuntimeError):
 
 class ss_debug_opts(ctypes.Structure):
     _fields_ = [("skip_mask", ctypes.c_void_p), ("vote_margin", ctypes.c_void_p),
-                ("count_only", ctypes.c_int)]
+                ("count_only", ctypes.c_int), ("fault_inject", ctypes.c_int)]
 
 
 class ss_problem(ctypes.Structure):
@@ -99,8 +99,9 @@ def _stream(stream):
     return stream.cuda_stream
 
 
-def _dbg(skip_mask=None, vote_margin=None, count_only=False):
-    return ss_debug_opts(_ptr(skip_mask), _ptr(vote_margin), int(bool(count_only)))
+def _dbg(skip_mask=None, vote_margin=None, count_only=False, fault_inject=0):
+    return ss_debug_opts(_ptr(skip_mask), _ptr(vote_margin), int(bool(count_only)),
+                         int(fault_inject))
 
 
 def ss_status_string(status: int) -> str:
@@ -136,8 +137,8 @@ def ss_attn_decode(q, k_cache, v_cache, o, B, Hq, Hkv, Lk, d, scale, lam, num_kv
 
 def ss_attn_decode_ex(q, k_cache, v_cache, o, B, Hq, Hkv, Lk, d, scale, lam, num_kv_splits,
                       skip_counts=None, workspace=None, workspace_bytes=0, skip_mask=None,
-                      vote_margin=None, count_only=False, stream=None) -> int:
-    dbg = _dbg(skip_mask, vote_margin, count_only)
+                      vote_margin=None, count_only=False, stream=None, fault_inject=0) -> int:
+    dbg = _dbg(skip_mask, vote_margin, count_only, fault_inject)
     return load().ss_attn_decode_ex(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), B, Hq, Hkv,
                                     Lk, d, float(scale), float(lam), int(num_kv_splits),
                                     _ptr(skip_counts), _ptr(workspace), int(workspace_bytes),

@@ -67,6 +67,7 @@ struct DecodeParams {
   float* margin;
   uint32_t* status;
   int count_only;
+  int fault_inject;  // test only: skip one K copy per split (bounded-wait expiry)
 };
 
 // Launchers (return a CUDA error code; arguments are already validated).

@@ -147,16 +147,20 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::kThreads, 1) decode_kernel(c
   }
   __syncthreads();
 
-  // Thread 0 owns every bulk copy.
-  int nk_issued = 0;
+  // Thread 0 owns every bulk copy; it records the newest tile issued into
+  // each K stage so that an aborted kernel waits for exactly those copies.
+  int k_last[kKStages];
+#pragma unroll
+  for (int s2 = 0; s2 < kKStages; ++s2) k_last[s2] = -1;
   uint32_t nv_issued[2] = {0u, 0u};
   auto issue_k = [&](int t) {
+    if (p.fault_inject == 1 && t == 1) return;  // test only: this copy never comes
     const int st = t % kKStages;
     const uint32_t bytes = static_cast<uint32_t>(tile_rows(t)) * D * 2;
     mbar_arrive_expect_tx(&ctl->k_full[st], bytes);
     bulk_load(sK + st * C::kTileBytes, kbase + static_cast<size_t>(j0 + t) * kTile * D, bytes,
               &ctl->k_full[st]);
-    nk_issued = t + 1;
+    k_last[st] = t;
   };
   if (tid == 0)
     for (int t = 0; t < min(nt, kKStages); ++t) issue_k(t);
@@ -459,11 +463,9 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::kThreads, 1) decode_kernel(c
   if (tid == 0) {
     if (*abort_flag) {
       // Let in-flight copies land before shared memory is released.
-      for (int s = 0; s < kKStages; ++s)
-        if (nk_issued > s) {
-          const int ik = s + ((nk_issued - 1 - s) / kKStages) * kKStages;
-          mbar_wait(&ctl->k_full[s], (ik / kKStages) & 1, nullptr);
-        }
+#pragma unroll
+      for (int s2 = 0; s2 < kKStages; ++s2)
+        if (k_last[s2] >= 0) mbar_wait(&ctl->k_full[s2], (k_last[s2] / kKStages) & 1, nullptr);
       for (int s = 0; s < 2; ++s)
         if (nv_issued[s] > 0) mbar_wait(&ctl->v_full[s], (nv_issued[s] - 1) & 1, nullptr);
       report_timeout(p.status);

@@ -186,6 +186,7 @@ ss_status decode_impl(const void* q, const void* k, const void* v, void* o, int 
   p.margin = dbg ? dbg->vote_margin : nullptr;
   p.status = status_ptr();
   p.count_only = count_only ? 1 : 0;
+  p.fault_inject = dbg ? dbg->fault_inject : 0;
   const Mode mode = count_only ? Mode::kCount : (dense ? Mode::kDense : Mode::kSparse);
   cudaError_t e = launch_decode(p, mode, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SS_OK : SS_ERR_CUDA;

@@ -82,6 +82,12 @@ typedef struct {
      Decisions equal those of the full pass: a skipped tile never raises the
      running max when lambda <= 1. */
   int count_only;
+  /* Test only, decode only (0 otherwise).  1: the copy of each split's
+     second K tile is never issued, so the kernel's bounded wait for it
+     expires (after about a second); the kernel then lets its other copies
+     land, returns, and ss_stream_status() reports SS_ERR_TIMEOUT.  The
+     output is unspecified; the context stays usable. */
+  int fault_inject;
 } ss_debug_opts;
 
 /*

@@ -104,6 +104,25 @@ def test_decode_rejects_before_launch(capi, kw, expect):
     assert st == getattr(capi, expect)
 
 
+def test_struct_layouts_match_the_header(capi, tmp_path):
+    """ctypes mirrors of the C structs have the C compiler's sizes and offsets."""
+    src = tmp_path / "sz.c"
+    src.write_text(
+        '#include <stdio.h>\n#include <stddef.h>\n#include "ssattn.h"\n'
+        "int main(void) {\n"
+        '  printf("%zu %zu %zu %zu %zu\\n", sizeof(ss_debug_opts), sizeof(ss_problem),\n'
+        "         offsetof(ss_debug_opts, fault_inject), offsetof(ss_problem, skip_counts),\n"
+        "         offsetof(ss_problem, stream));\n"
+        "  return 0;\n}\n")
+    exe = tmp_path / "sz"
+    subprocess.check_call(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)])
+    got = [int(x) for x in subprocess.check_output([str(exe)], text=True).split()]
+    want = [ctypes.sizeof(capi.ss_debug_opts), ctypes.sizeof(capi.ss_problem),
+            capi.ss_debug_opts.fault_inject.offset, capi.ss_problem.skip_counts.offset,
+            capi.ss_problem.stream.offset]
+    assert got == want
+
+
 def test_workspace_size(capi):
     assert capi.ss_attn_decode_workspace_size(64, 32, 128, 1) == 0
     assert capi.ss_attn_decode_workspace_size(64, 32, 128, 8) == 64 * 32 * 8 * 130 * 4
