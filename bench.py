@@ -352,6 +352,164 @@ def run_native(args):
         dist.destroy_process_group()
 
 
+def _time_ms(fn, iters=10, warmup=3):
+    import torch
+
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(iters):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    ts.sort()
+    return ts[len(ts) // 2]
+
+
+def run_suite(args):
+    """Every workload of the plan: calibrated sparsity points, dense path,
+    (A, B) fits, and the calibration-stability sweep.  One JSON line each."""
+    import numpy as np
+    import torch
+
+    import block_sparse_attention_sm_gb300 as ss
+    from block_sparse_attention_sm_gb300 import synth
+
+    ss.build()
+    peaks = _peaks()
+    dev = torch.device("cuda", 0)
+
+    def emit(d):
+        print(json.dumps(d), flush=True)
+
+    def prefill_points(name, targets):
+        inp, cfg = synth.make(name, seed=0, device=dev)
+        q, k, v = inp.q, inp.k, inp.v
+        B, Hq, Lq, d = q.shape
+        Lk = k.shape[2]
+        nqb, nT = -(-Lq // TILE), -(-Lk // TILE)
+        cnt = torch.zeros(B * Hq * nqb, dtype=torch.int32, device=dev)
+        o = torch.empty_like(q)
+        # evaluated (unit, tile) pairs: causal blocks stop at the diagonal
+        per_head = 0
+        for qb in range(nqb):
+            rows = min(TILE, Lq - qb * TILE)
+            last = qb * TILE + rows - 1 + (Lk - Lq)
+            per_head += (min(nT, last // TILE + 1) if cfg["causal"] else nT) if last >= 0 else 0
+        n_eval = per_head * B * Hq
+        dense_eq = 4.0 * B * Hq * Lq * Lk * d * (0.5 if cfg["causal"] else 1.0)
+        fit_s, fit_a, dense_ms = [], [], None
+        for s_t in targets:
+            a = 0.0
+            if s_t > 0:
+                a, _ = ss.calibrate("prefill", q, k, v, scale=cfg["scale"], target_sparsity=s_t,
+                                    causal=cfg["causal"])
+            lam = min(1.0, a / Lk)
+            ms = _time_ms(lambda: ss.prefill(q, k, v, scale=cfg["scale"], causal=cfg["causal"],
+                                             lam=lam, counts=cnt, out=o))
+            sk = int(cnt.sum())
+            kept = n_eval - sk
+            flops = 2.0 * TILE * TILE * d * (n_eval + kept)
+            if s_t == 0:
+                dense_ms = ms
+            if s_t > 0 and a > 0:
+                fit_s.append(sk / n_eval)
+                fit_a.append(a)
+            emit({"suite": name, "kind": "prefill", "target": s_t, "a": a, "lambda": lam,
+                  "sparsity": round(sk / n_eval, 4), "ms": round(ms, 4),
+                  "tflops_executed": round(flops / ms / 1e9, 1),
+                  "tflops_dense_equivalent": round(dense_eq / ms / 1e9, 1),
+                  "frac_of_peak": round(flops / ms / 1e9 / peaks["bf16"], 4),
+                  "speedup_vs_dense": round(dense_ms / ms, 3) if dense_ms else None})
+        if len(fit_s) >= 2:
+            A, Bc = ss.fit_factor(fit_s, fit_a)
+            emit({"suite": name, "kind": "fit", "A": A, "B": Bc, "points": list(zip(fit_s, fit_a))})
+        del q, k, v, o, inp
+        torch.cuda.empty_cache()
+
+    def decode_points(name, targets):
+        inp, cfg = synth.make(name, seed=0, device=dev)
+        q, k, v = inp.q, inp.k, inp.v
+        B, Hq, d = q.shape
+        Hkv, Lk = k.shape[1], k.shape[2]
+        S = cfg["num_splits"]
+        nT = -(-Lk // TILE)
+        cnt = torch.zeros(B * Hkv * S, dtype=torch.int32, device=dev)
+        o = torch.empty_like(q)
+        wsb, _ = ss.decode_workspace(B, Hq, d, S, dev)
+        n_eval = B * Hkv * nT
+        fit_s, fit_a, dense_ms = [], [], None
+        for s_t in targets:
+            a = 0.0
+            if s_t > 0:
+                a, _ = ss.calibrate("decode", q, k, v, scale=cfg["scale"], target_sparsity=s_t,
+                                    num_kv_splits=S)
+            lam = min(1.0, a / Lk)
+            ms = _time_ms(lambda: ss.decode(q, k, v, scale=cfg["scale"], lam=lam, num_kv_splits=S,
+                                            counts=cnt, out=o, workspace=wsb))
+            sk = int(cnt.sum())
+            kept = n_eval - sk
+            byts = B * Hkv * Lk * d * 2 + kept * TILE * d * 2 + 2 * B * Hq * d * 2
+            if s_t == 0:
+                dense_ms = ms
+            if s_t > 0 and a > 0:
+                fit_s.append(sk / n_eval)
+                fit_a.append(a)
+            emit({"suite": name, "kind": "decode", "target": s_t, "a": a, "lambda": lam,
+                  "sparsity": round(sk / n_eval, 4), "ms": round(ms, 4),
+                  "gbs": round(byts / ms / 1e6, 1), "frac_of_peak": round(byts / ms / 1e6 / peaks["hbm"], 4),
+                  "tokens_per_s": round(B / ms * 1e3, 1),
+                  "speedup_vs_dense": round(dense_ms / ms, 3) if dense_ms else None})
+        if len(fit_s) >= 2:
+            A, Bc = ss.fit_factor(fit_s, fit_a)
+            emit({"suite": name, "kind": "fit", "A": A, "B": Bc, "points": list(zip(fit_s, fit_a))})
+        del q, k, v, o, inp
+        torch.cuda.empty_cache()
+
+    def stability(target=0.7, ref_L=32768):
+        """Calibrate a at one length, then hold a (lambda = a/L) or hold lambda
+        fixed and measure the skipped fraction at other lengths.  Count-only."""
+        from block_sparse_attention_sm_gb300 import capi
+
+        Ls = [4096, 8192, 16384, 32768, 65536, 131072]
+        res = {}
+        for L in Ls:
+            inp = synth.decode_inputs(B=8, Hq=32, Hkv=8, Lk=L, d=128, hot_frac=0.10, seed=3,
+                                      device=dev)
+            res[L] = inp
+        q, k, v = res[ref_L].q, res[ref_L].k, res[ref_L].v
+        scale = 128 ** -0.5
+        a, _ = ss.calibrate("decode", q, k, v, scale=scale, target_sparsity=target, num_kv_splits=1)
+        lam_fixed = a / ref_L
+        for L in Ls:
+            inp = res[L]
+            nT = -(-L // TILE)
+            cnt = torch.zeros(8 * 8, dtype=torch.int32, device=dev)
+            out = {}
+            for tag, lam in (("lambda_a_over_L", min(1.0, a / L)), ("fixed_lambda", lam_fixed)):
+                st = capi.ss_attn_decode_ex(inp.q, inp.k, inp.v, None, 8, 32, 8, L, 128, scale, lam,
+                                            1, cnt, None, 0, count_only=True)
+                assert st == capi.SS_OK
+                torch.cuda.synchronize()
+                out[tag] = round(int(cnt.sum()) / (64 * nT), 4)
+            emit({"suite": "calibration_stability", "L": L, "a": a, "calibrated_at": ref_L,
+                  "target": target, **out})
+        del res
+        torch.cuda.empty_cache()
+
+    prefill_points("tiny_prefill", [0.0, 0.5, 0.75])
+    prefill_points("dit_prefill_32k", [0.0, 0.5, 0.7])
+    prefill_points("llama_prefill_16k", [0.0, 0.5, 0.7])
+    decode_points("llama_decode_32k", [0.0, 0.5, 0.7])
+    prefill_points("long_prefill_128k", [0.0, 0.5, 0.7, 0.9])
+    decode_points("long_decode_128k", [0.0, 0.5, 0.7, 0.9])
+    stability()
+
+
 def cpu_baseline(q, k, v, cfg, lam, seconds_budget):
     """Time the fp64 oracle (as it stands) on whole query blocks of the
     prefill workload; report executed TFLOP/s on the same FLOP count."""
@@ -462,6 +620,8 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--suite", action="store_true",
+                    help="measure every workload (calibrated sweeps, fits, stability); JSON lines")
     ap.add_argument("--profile", action="store_true",
                     help="run calibration + the timed loop only (for ncu); prints nothing")
     ap.add_argument("--prefill-heads", type=int, default=0,
@@ -473,6 +633,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.suite:
+        run_suite(args)
     else:
         run_native(args)
 
