@@ -57,9 +57,7 @@ struct DecodeParams {
   float scale_log2;
   float scale;
   float thr_raw;
-  const __nv_bfloat16* q;
-  const __nv_bfloat16* k;
-  const __nv_bfloat16* v;
+  const __nv_bfloat16* q;  // [B][Hq][d]; K and V are read through tensor maps
   __nv_bfloat16* o;       // final output when S == 1
   float* part;            // [B*Hq][S][d + 2] partial (O..., m, l) when S > 1
   uint32_t* counts;
@@ -73,6 +71,7 @@ struct DecodeParams {
 // Launchers (return a CUDA error code; arguments are already validated).
 cudaError_t launch_prefill(int d, Mode mode, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, const PrefillParams& p, cudaStream_t st);
-cudaError_t launch_decode(const DecodeParams& p, Mode mode, cudaStream_t st);
+cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
+                          Mode mode, cudaStream_t st);
 
 }  // namespace ssattn

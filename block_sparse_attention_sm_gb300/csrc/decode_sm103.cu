@@ -4,25 +4,30 @@
 // Method (BLASST summary, §Methodologie and §Kernel-ontwerp; "Skip-Softmax"
 // design doc, §The skip test): decode is bound by HBM traffic.  Every K tile
 // of a split is streamed (the scores decide the skip), but a skipped tile's
-// V block is never loaded.  To keep the pipeline free of bubbles the
-// decisions are taken a chunk of tiles at a time and the surviving V tiles of
-// that chunk are fetched as one batch, while the next chunk's scores run.
+// V block is never loaded; the V tiles of kept tiles are fetched as soon as
+// the vote has decided, while the following K tiles keep streaming.
 //
-// One CTA = one (sequence b, KV head, split); 512 threads (256 for 8-row groups).  The G
-// query heads sharing the KV head (one token each) form the voting group:
-// a tile is skipped only if every one of them passes the test.
+// One CTA = one (sequence b, KV head, split); 256 threads in 8 warps:
+//   warps 0-3  vote / softmax: thread i = TMEM lane i, which is key i of the
+//              tile for the scores and dimension i for the P.V result.
+//   warp 4     TMA producer of the K ring (NK stages, 128-byte swizzle).
+//   warp 5     TMA producer of the V slots (kept tiles only, in kept order).
+//   warp 6     TMEM allocator + issuer of the score MMAs
+//              S^T = K_tile . Q^T  (M = 128 keys, N = 16/32 query rows
+//              padded with zero rows, K = d), fp32 in TMEM.
+//   warp 7     issuer of the value MMAs  O_i^T = V_i^T . P_i^T
+//              (M = 128 = d, N = query rows, K = 128 keys), one fresh TMEM
+//              accumulator per kept tile.
+// The G query heads that share the KV head (one token each) are the voting
+// group: a tile is skipped only if every one of them passes the test.  The
+// contraction has only G rows, but putting it on the tensor cores takes it
+// off the issue slots, which bound the CUDA-core version of this kernel.
 //
-// Pipeline per chunk c of 2 tiles (iteration c), two block barriers:
-//   A(c)    scores of tiles 2c, 2c+1 (each by half of the warps) from the K
-//           ring (4 stages, 1-D bulk copies of contiguous 128-key tiles),
-//           plus per-warp partial row maxima;
-//   -- barrier; the two freed K stages are refilled 2 chunks ahead;
-//   vote(c) one warp (lane = row): tile maxima, the vote with the exact
-//           running maximum, counters / mask / margin, survivor list;
-//   C(c-1)  meanwhile, online softmax + P.V over chunk c-1's survivors;
-//   -- barrier; the batch of V loads for chunk c's survivors is issued.
-// Scores use fp32 FMAs on bf16 K read from shared memory (the contraction
-// has only G <= 8 rows; the kernel is bound by the K stream, not by math).
+// Online softmax: the vote and the exponentials use the exact running
+// maximum m.  P_i = exp2((s - m_i) * scale * log2e) with m_i the maximum after
+// kept tile i; each thread (dimension) folds the kept tiles' P.V results into
+// registers in kept order, acc = acc * exp2(m_prev - m_i) + O_i, and keeps a
+// per-key partial row sum l rescaled the same way.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -32,94 +37,119 @@ namespace ssattn {
 
 namespace {
 
-constexpr int kKStages = 4;
-
-struct DecodeCtl {
-  uint64_t k_full[kKStages];
-  uint64_t v_full[2];
-  int abort_flag;
-  int n_surv[2];           // [chunk parity]
-  int surv_tile[2][2];     // [chunk parity][slot]
-  uint32_t surv_par[2][2];
-};
+constexpr int kDecThreads = 256;
+constexpr int kWarpK = 4, kWarpV = 5, kWarpS = 6, kWarpPV = 7;
 
 template <int D, int GP>
-struct DecodeCfg {
-  // 16 warps (8 per tile of a chunk) hide shared-memory latency; the
-  // 8-row vote group keeps 8 warps to stay within the register budget.
-  static constexpr int kThreads = (GP >= 8) ? 256 : 512;
-  static constexpr int kWarpsPerTile = kThreads / 64;
-  static constexpr int kKeysPerWarp = kTile / kWarpsPerTile;
+struct DecCfg {
+  static constexpr int NQ = (GP <= 16) ? 16 : 32;  // MMA N (rows padded with zeros)
+  static constexpr int NK = (D == 128) ? 4 : 8;    // K ring stages
+  static constexpr int NV = (D == 128) ? 2 : 4;    // V / P / O slots
+  static constexpr int NS = 4;                      // score buffers in TMEM
+  static constexpr int kChunks = D / 64;            // 128-byte swizzle chunks per row
   static constexpr int kTileBytes = kTile * D * 2;
-  static constexpr int kLPR = D / 16;          // lanes per key row (two 16-byte chunks each)
-  static constexpr int kKPI = 32 / kLPR;       // keys per warp iteration
-  static constexpr int kIters = kKeysPerWarp / kKPI;  // iterations for the warp's keys
-  static constexpr int kNDP = D / 2;           // threads per key group in P.V (bf16 pairs)
-  static constexpr int kNKG = kThreads / kNDP;  // key groups
-  static constexpr int kKPG = kTile / kNKG;    // keys per group
-  // shared memory layout (bytes, 16-byte aligned pieces)
-  static constexpr int kKOff = 0;
-  static constexpr int kVOff = kKOff + kKStages * kTileBytes;
-  static constexpr int kQOff = kVOff + 2 * kTileBytes;                 // float [GP][D]
-  static constexpr int kScOff = kQOff + GP * D * 4;                    // float [2][2][GP][128]
-  static constexpr int kPOff = kScOff + 2 * 2 * GP * kTile * 4;        // float [2][128][GP]
-  static constexpr int kTmOff = kPOff + 2 * kTile * GP * 4;            // float [2][2][GP]
-  static constexpr int kAlOff = kTmOff + 2 * 2 * GP * 4;               // float [2][GP]
-  static constexpr int kMlOff = kAlOff + 2 * GP * 4;                   // float [GP][2]
-  static constexpr int kPmOff = kMlOff + GP * 2 * 4;                   // float [2][2][WPT][GP]
-  static constexpr int kCtlOff = (kPmOff + 2 * 2 * kWarpsPerTile * GP * 4 + 15) / 16 * 16;
-  static constexpr int kVoteWarp = kThreads / 32 - 1;
-  static constexpr int kSmemBytes = kCtlOff + 128;
-  static_assert(sizeof(DecodeCtl) <= 128, "control block overflow");
-  static_assert(kNKG * GP * D * 4 <= kKStages * kTileBytes, "reduction buffer must fit the K ring");
+  static constexpr int kQBytes = NQ * D * 2;
+  static constexpr int kPBytes = NQ * kTile * 2;
+  // V slots first: for d = 64 the value MMA (M = 128) reads a second,
+  // unused 64-row atom 16 KB past its slot, which must stay inside the block.
+  static constexpr int kVOff = 0;
+  static constexpr int kKOff = kVOff + NV * kTileBytes;
+  static constexpr int kQOff = kKOff + NK * kTileBytes;
+  static constexpr int kPOff = kQOff + kQBytes;
+  static constexpr int kRedOff = kPOff + NV * kPBytes;            // float [2][GP][4]
+  static constexpr int kLRedOff = kRedOff + 2 * GP * 4 * 4;       // float [GP][4]
+  static constexpr int kMsOff = kLRedOff + GP * 4 * 4;            // float [2 NV][GP]
+  static constexpr int kCtlOff = (kMsOff + 2 * NV * GP * 4 + 15) / 16 * 16;
+  static constexpr int kCtlBytes = 512;
+  static constexpr int kSmemBytes = kCtlOff + kCtlBytes + 1024;  // + alignment slack
+  static constexpr uint32_t kColS = 0;              // S buffer b at kColS + NQ b
+  static constexpr uint32_t kColO = NS * NQ;        // O slot s at kColO + NQ s
+  static constexpr uint32_t kTmemCols = ((NS + NV) * NQ <= 128) ? 128 : 256;
+  static_assert((NS + NV) * NQ <= kTmemCols, "TMEM columns");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+  static_assert(D != 64 || NV * kTileBytes + 16384 <= kKOff + NK * kTileBytes, "d=64 atom");
 };
 
+template <int NK, int NV, int NS>
+struct DecCtl {
+  uint64_t k_full[NK], k_empty[NK];
+  uint64_t s_full[NS], s_empty[NS];
+  uint64_t v_full[NV], slot_free[NV], vq_full[NV], p_full[NV];
+  uint64_t s_done, pv_done;
+  int kq[NV];    // kept tile for the V producer (-1: no more)
+  int prec[NV];  // 1: P written, 0: no more (value-MMA issuer)
+  uint32_t tmem_base;
+  int abort_flag;
+};
 
-// Packed fp32 pair arithmetic (two IEEE fp32 FMAs per instruction).
-__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
+// tcgen05.ld of N consecutive fp32 columns of the warp's 32 lanes.
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&r)[N]);
+template <>
+__device__ __forceinline__ void tmem_ld_cols<1>(uint32_t taddr, float (&r)[1]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=f"(r[0]) : "r"(taddr));
 }
-__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
-  return static_cast<uint64_t>(__float_as_uint(lo)) | (static_cast<uint64_t>(__float_as_uint(hi)) << 32);
+template <>
+__device__ __forceinline__ void tmem_ld_cols<2>(uint32_t taddr, float (&r)[2]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];"
+               : "=f"(r[0]), "=f"(r[1])
+               : "r"(taddr));
 }
-// bf16 pair (one 32-bit word) -> fp32 pair (exact: bf16 is the upper half).
-__device__ __forceinline__ uint64_t bf16x2_to_f32x2(uint32_t w) {
-  return static_cast<uint64_t>(w << 16) | (static_cast<uint64_t>(w & 0xffff0000u) << 32);
+template <>
+__device__ __forceinline__ void tmem_ld_cols<4>(uint32_t taddr, float (&r)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(r[0]), "=f"(r[1]), "=f"(r[2]), "=f"(r[3])
+               : "r"(taddr));
 }
-__device__ __forceinline__ float f32x2_sum(uint64_t v) {
-  return __uint_as_float(static_cast<uint32_t>(v)) + __uint_as_float(static_cast<uint32_t>(v >> 32));
+template <>
+__device__ __forceinline__ void tmem_ld_cols<8>(uint32_t taddr, float (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=f"(r[0]), "=f"(r[1]), "=f"(r[2]), "=f"(r[3]), "=f"(r[4]), "=f"(r[5]),
+                 "=f"(r[6]), "=f"(r[7])
+               : "r"(taddr));
+}
+template <>
+__device__ __forceinline__ void tmem_ld_cols<16>(uint32_t taddr, float (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=f"(r[0]), "=f"(r[1]), "=f"(r[2]), "=f"(r[3]), "=f"(r[4]), "=f"(r[5]), "=f"(r[6]),
+        "=f"(r[7]), "=f"(r[8]), "=f"(r[9]), "=f"(r[10]), "=f"(r[11]), "=f"(r[12]), "=f"(r[13]),
+        "=f"(r[14]), "=f"(r[15])
+      : "r"(taddr));
 }
 
-__device__ __forceinline__ void bf16x8_to_f32(const uint4& raw, float (&f)[8]) {
-  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(w[i] << 16);
-    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-  }
+// Maximum over the warp (every lane gets it).
+__device__ __forceinline__ float warp_max(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
 }
 
 template <int D, int GP, Mode MODE>
-__global__ void __launch_bounds__(DecodeCfg<D, GP>::kThreads, 1) decode_kernel(const DecodeParams p) {
-  using C = DecodeCfg<D, GP>;
-  constexpr int kDecThreads = C::kThreads;
+__global__ void __launch_bounds__(kDecThreads, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                  const DecodeParams p) {
+  using C = DecCfg<D, GP>;
+  constexpr int NK = C::NK, NV = C::NV, NS = C::NS, NQ = C::NQ;
   constexpr bool kPV = (MODE != Mode::kCount);
   constexpr bool kVote = (MODE != Mode::kDense);
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* sK = smem + C::kKOff;
+  constexpr bool kDenseV = (MODE == Mode::kDense);  // every tile kept: V needs no decision
+  using Ctl = DecCtl<NK, NV, NS>;
+  static_assert(sizeof(Ctl) <= C::kCtlBytes, "control block overflow");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
   uint8_t* sV = smem + C::kVOff;
-  float* sQ = reinterpret_cast<float*>(smem + C::kQOff);
-  float* sSc = reinterpret_cast<float*>(smem + C::kScOff);
-  float* sP = reinterpret_cast<float*>(smem + C::kPOff);
-  float* sTm = reinterpret_cast<float*>(smem + C::kTmOff);
-  float* sAl = reinterpret_cast<float*>(smem + C::kAlOff);
-  float* sMl = reinterpret_cast<float*>(smem + C::kMlOff);
-  float* sPm = reinterpret_cast<float*>(smem + C::kPmOff);
-  auto* ctl = reinterpret_cast<DecodeCtl*>(smem + C::kCtlOff);
+  uint8_t* sK = smem + C::kKOff;
+  uint8_t* sQ = smem + C::kQOff;
+  uint8_t* sP = smem + C::kPOff;
+  float* sRed = reinterpret_cast<float*>(smem + C::kRedOff);
+  float* sLRed = reinterpret_cast<float*>(smem + C::kLRedOff);
+  float* sMs = reinterpret_cast<float*>(smem + C::kMsOff);
+  auto* ctl = reinterpret_cast<Ctl*>(smem + C::kCtlOff);
   volatile int* abort_flag = &ctl->abort_flag;
-  auto SC = [&](int buf, int tl, int g) { return sSc + ((buf * 2 + tl) * GP + g) * kTile; };
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = p.G;
@@ -128,349 +158,358 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::kThreads, 1) decode_kernel(c
   const int b = bk / p.Hkv, kvh = bk - (bk / p.Hkv) * p.Hkv;
   const int j0 = split * p.T;
   const int nt = max(0, min(p.nT, j0 + p.T) - j0);
-  const int nchunks = (nt + 1) / 2;
-  const __nv_bfloat16* kbase = p.k + (static_cast<size_t>(bk) * p.Lk) * D;
-  const __nv_bfloat16* vbase = p.v + (static_cast<size_t>(bk) * p.Lk) * D;
   auto tile_rows = [&](int t) { return min(kTile, p.Lk - (j0 + t) * kTile); };
 
-  if (tid == 0) {
-    for (int s = 0; s < kKStages; ++s) mbar_init(&ctl->k_full[s], 1);
-    for (int s = 0; s < 2; ++s) mbar_init(&ctl->v_full[s], 1);
-    ctl->abort_flag = 0;
-    ctl->n_surv[0] = ctl->n_surv[1] = 0;
-    fence_mbar_init();
-  }
-  // Query rows of the group (fp32 copy; padding rows are zero).
-  for (int idx = tid; idx < GP * D; idx += kDecThreads) {
-    const int g = idx / D, e = idx - (idx / D) * D;
-    sQ[idx] = (g < G) ? __bfloat162float(p.q[(static_cast<size_t>(b) * p.Hq + kvh * G + g) * D + e]) : 0.f;
-  }
-  __syncthreads();
-
-  // Thread 0 owns every bulk copy; it records the newest tile issued into
-  // each K stage so that an aborted kernel waits for exactly those copies.
-  int k_last[kKStages];
-#pragma unroll
-  for (int s2 = 0; s2 < kKStages; ++s2) k_last[s2] = -1;
-  uint32_t nv_issued[2] = {0u, 0u};
+  // ------------------------------------------------------------------ setup
+  int n_k_issued = 0;  // K producer bookkeeping (teardown)
   auto issue_k = [&](int t) {
+    const int st = t % NK;
     if (p.fault_inject == 1 && t == 1) return;  // test only: this copy never comes
-    const int st = t % kKStages;
-    const uint32_t bytes = static_cast<uint32_t>(tile_rows(t)) * D * 2;
-    mbar_arrive_expect_tx(&ctl->k_full[st], bytes);
-    bulk_load(sK + st * C::kTileBytes, kbase + static_cast<size_t>(j0 + t) * kTile * D, bytes,
-              &ctl->k_full[st]);
-    k_last[st] = t;
+    mbar_arrive_expect_tx(&ctl->k_full[st], C::kTileBytes);
+#pragma unroll
+    for (int c = 0; c < C::kChunks; ++c)
+      tma_load_3d(sK + st * C::kTileBytes + c * 16384, &tmK, &ctl->k_full[st], c * 64,
+                  (j0 + t) * kTile, bk);
+    n_k_issued = t + 1;
   };
-  if (tid == 0)
-    for (int t = 0; t < min(nt, kKStages); ++t) issue_k(t);
-
-  // Per-lane query slice for the score phase: the lane owns 16 dimensions,
-  // chunks c and c + kLPR of eight (c = lane % kLPR), as fp32 pairs.
-  uint64_t qp[GP][8];
-  {
-    const int e0 = (lane % C::kLPR) * 8, e1 = e0 + C::kLPR * 8;
-#pragma unroll
-    for (int g = 0; g < GP; ++g)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        qp[g][j] = pack_f32x2(sQ[g * D + e0 + 2 * j], sQ[g * D + e0 + 2 * j + 1]);
-        qp[g][4 + j] = pack_f32x2(sQ[g * D + e1 + 2 * j], sQ[g * D + e1 + 2 * j + 1]);
-      }
+  if (warp == kWarpK && lane == 0) {
+    for (int s = 0; s < NK; ++s) {
+      mbar_init(&ctl->k_full[s], 1);
+      mbar_init(&ctl->k_empty[s], 1);
+    }
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&ctl->s_full[s], 1);
+      mbar_init(&ctl->s_empty[s], 4);
+    }
+    for (int s = 0; s < NV; ++s) {
+      mbar_init(&ctl->v_full[s], 1);
+      mbar_init(&ctl->slot_free[s], 1);
+      mbar_init(&ctl->vq_full[s], 1);
+      mbar_init(&ctl->p_full[s], 4);
+    }
+    mbar_init(&ctl->s_done, 1);
+    mbar_init(&ctl->pv_done, 1);
+    ctl->abort_flag = 0;
+    fence_mbar_init();
+    // The first K tiles go out before anything else is set up.
+    tma_prefetch_desc(&tmK);
+    for (int t = 0; t < min(nt, NK); ++t) issue_k(t);
   }
-
-  // Running state.  Vote warp, lane g: exact running max of row g.
-  // Warp g (< GP): softmax state of row g (all lanes hold the same values).
-  float mt = -INFINITY;
-  float m_run = -INFINITY, l_run = 0.f;
-  float acc[GP][2];
-#pragma unroll
-  for (int g = 0; g < GP; ++g) acc[g][0] = acc[g][1] = 0.f;
-  uint32_t skipped = 0;
-  const float sl2 = p.scale_log2;
-
-  for (int c = 0; c <= nchunks; ++c) {
-    const int cb = c & 1;
-    // ---------------------------------------------------------------- A(c)
-    // Scores of tiles 2c, 2c+1 (half of the warps each), plus each warp's
-    // partial row maxima for the vote.
-    if (c < nchunks) {
-      const int tl = warp / C::kWarpsPerTile;
-      const int t = 2 * c + tl;
-      if (t < nt) {
-        const int st = t % kKStages;
-        // warp-uniform: the loop below shuffles across the whole warp
-        if (__all_sync(0xffffffffu, mbar_wait(&ctl->k_full[st], (t / kKStages) & 1, abort_flag))) {
-          const uint8_t* kt = sK + st * C::kTileBytes;
-          const int valid = tile_rows(t);
-          float* sc = SC(cb, tl, 0);
-          float rmax[GP];
-#pragma unroll
-          for (int j = 0; j < GP; ++j) rmax[j] = -INFINITY;
-          int gsel = 0, n = GP;
-          bool writer = true;
-#pragma unroll 2
-          for (int it = 0; it < C::kIters; ++it) {
-            const int key = (warp % C::kWarpsPerTile) * C::kKeysPerWarp + it * C::kKPI + lane / C::kLPR;
-            // Two 16-byte chunks of the key row.  For d = 128 the first load
-            // of the warp covers bytes [0,128) of its four rows (all eight
-            // bank groups); for d = 64 the chunk order alternates with the
-            // key's parity for the same reason.
-            const int cc = lane % C::kLPR;
-            const bool swap = (D == 64) && (key & 1);
-            const uint8_t* row = kt + key * D * 2;
-            const uint4 r0 = *reinterpret_cast<const uint4*>(row + (swap ? cc + C::kLPR : cc) * 16);
-            const uint4 r1 = *reinterpret_cast<const uint4*>(row + (swap ? cc : cc + C::kLPR) * 16);
-            const uint4 ra = swap ? r1 : r0, rb = swap ? r0 : r1;
-            const uint32_t w[8] = {ra.x, ra.y, ra.z, ra.w, rb.x, rb.y, rb.z, rb.w};
-            uint64_t kp[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) kp[j] = bf16x2_to_f32x2(w[j]);
-            float part[GP];
-#pragma unroll
-            for (int g = 0; g < GP; ++g) {
-              uint64_t a = 0;
-#pragma unroll
-              for (int j = 0; j < 8; ++j) a = ffma2(qp[g][j], kp[j], a);
-              part[g] = f32x2_sum(a);
-            }
-            // Transpose-reduce over the kLPR lanes of this key: each halving
-            // step hands half of the rows to the partner lane, so the lane
-            // ends up holding the full dot products of rows gsel .. gsel+n-1
-            // (n > 1 only when a key has fewer lanes than the group rows).
-            gsel = 0;
-            n = GP;
-            writer = true;
-#pragma unroll
-            for (int o = C::kLPR / 2; o >= 1; o >>= 1) {
-              const bool upper = (lane & o) != 0;
-              if (n > 1) {
-                const int hn = n / 2;
-#pragma unroll
-                for (int j = 0; j < GP / 2; ++j) {
-                  if (j < hn) {
-                    const float send = upper ? part[j] : part[j + hn];
-                    const float keep = upper ? part[j + hn] : part[j];
-                    part[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-                  }
-                }
-                gsel += upper ? hn : 0;
-                n = hn;
-              } else {
-                part[0] += __shfl_xor_sync(0xffffffffu, part[0], o);
-                writer = writer && !upper;
-              }
-            }
-#pragma unroll
-            for (int j = 0; j < GP; ++j) {
-              if (j < n) {
-                const float sv = (key < valid) ? part[j] : -INFINITY;
-                rmax[j] = fmaxf(rmax[j], sv);
-                if (writer && gsel + j < G) sc[(gsel + j) * kTile + key] = sv;
-              }
-            }
-          }
-          // Partial maxima of this warp's keys: combine over the lanes that
-          // hold the same rows for different keys.
-#pragma unroll
-          for (int j = 0; j < GP; ++j) {
-            if (j < n) {
-#pragma unroll
-              for (int o = C::kLPR; o < 32; o <<= 1) rmax[j] = fmaxf(rmax[j], __shfl_xor_sync(0xffffffffu, rmax[j], o));
-              if (lane < C::kLPR && writer && gsel + j < G)
-                sPm[((cb * 2 + tl) * C::kWarpsPerTile + warp % C::kWarpsPerTile) * GP + gsel + j] = rmax[j];
-            }
-          }
-        }
-      }
-    }
-    __syncthreads();
-    if (tid == 0 && !*abort_flag) {
-      // Refill the stages the two tiles of this chunk just released.
-      for (int t = 2 * c + kKStages; t < min(nt, 2 * c + kKStages + 2); ++t) issue_k(t);
-    }
-
-    // ---------------------------------------------------------------- vote(c)
-    // One warp, lane g = row g: tile maxima from the partials, the vote with
-    // the exact running maximum, counters and the survivor list of chunk c.
-    if (c < nchunks && warp == C::kVoteWarp) {
-      int ns = 0;
-      for (int tl = 0; tl < 2; ++tl) {
-        const int t = 2 * c + tl;
-        if (t >= nt) break;
-        float tm = -INFINITY;
-        if (lane < G)
-#pragma unroll
-          for (int w2 = 0; w2 < C::kWarpsPerTile; ++w2)
-            tm = fmaxf(tm, sPm[((cb * 2 + tl) * C::kWarpsPerTile + w2) * GP + lane]);
-        float cval = -INFINITY;
-        if (lane < G && tm != -INFINITY) cval = (mt == -INFINITY) ? INFINITY : tm - mt;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) cval = fmaxf(cval, __shfl_xor_sync(0xffffffffu, cval, o));
-        const bool skip = kVote && (cval < p.thr_raw);
-        if (lane < G) {
-          mt = fmaxf(mt, tm);
-          sTm[(cb * 2 + tl) * GP + lane] = tm;
-        }
-        if (lane == 0) {
-          const long gi = static_cast<long>(bk) * p.nT + j0 + t;
-          if (p.mask != nullptr) p.mask[gi] = skip ? 1 : 0;
-          if (p.margin != nullptr) p.margin[gi] = (cval == INFINITY) ? INFINITY : cval * p.scale;
-          if (skip) ++skipped;
-          else if (kPV) ctl->surv_tile[cb][ns] = t;
-        }
-        if (!skip && kPV) ++ns;
-      }
-      if (lane == 0) ctl->n_surv[cb] = ns;
-    }
-
-    // ---------------------------------------------------------------- C(c-1)
-    // Online softmax + P.V over the survivors of chunk c-1 (their V tiles
-    // were fetched after the previous iteration's barrier).
-    if (kPV && c >= 1) {
-      const int pc = c - 1, pcb = pc & 1;
-      const int ns = ctl->n_surv[pcb];
-      if (ns > 0) {
-        bool ok = true;
-        for (int s2 = 0; s2 < ns; ++s2)
-          ok = ok && mbar_wait(&ctl->v_full[s2], ctl->surv_par[pcb][s2], abort_flag);
-        if (warp < GP) {
-          const int g = warp;
-          for (int s2 = 0; s2 < ns; ++s2) {
-            const int tl = ctl->surv_tile[pcb][s2] - 2 * pc;
-            float* prow = sP + s2 * kTile * GP;
-            if (g < G) {
-              const float tm = sTm[(pcb * 2 + tl) * GP + g];
-              const float m_new = fmaxf(m_run, tm);
-              const float alpha = (m_run == -INFINITY) ? 0.f : ex2_approx((m_run - m_new) * sl2);
-              const float mb = (m_new == -INFINITY) ? 0.f : m_new * sl2;
-              const float* sc = SC(pcb, tl, g);
-              float sum = 0.f;
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const int k = lane + 32 * kk;
-                const float pv = ex2_approx(fmaf(sc[k], sl2, -mb));
-                prow[k * GP + g] = pv;
-                sum += pv;
-              }
-#pragma unroll
-              for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-              l_run = alpha * l_run + sum;
-              m_run = m_new;
-              if (lane == 0) sAl[s2 * GP + g] = alpha;
-            } else {
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk) prow[(lane + 32 * kk) * GP + g] = 0.f;
-              if (lane == 0) sAl[s2 * GP + g] = 1.f;
-            }
-          }
-        }
-        __syncthreads();
-        if (ok) {
-          const int dp = tid % C::kNDP, kg = tid / C::kNDP;
-          for (int s2 = 0; s2 < ns; ++s2) {
-#pragma unroll
-            for (int g = 0; g < GP; ++g) {
-              const float a = sAl[s2 * GP + g];
-              acc[g][0] *= a;
-              acc[g][1] *= a;
-            }
-            const int valid = tile_rows(ctl->surv_tile[pcb][s2]);
-            const uint8_t* vt = sV + s2 * C::kTileBytes;
-            const float* prow = sP + s2 * kTile * GP;
-            const int k0 = kg * C::kKPG;
-            const int kend = min(C::kKPG, valid - k0);
-#pragma unroll 4
-            for (int kk = 0; kk < kend; ++kk) {
-              const int k = k0 + kk;
-              const uint32_t wv = *reinterpret_cast<const uint32_t*>(vt + k * D * 2 + dp * 4);
-              const float v0 = __uint_as_float(wv << 16), v1 = __uint_as_float(wv & 0xffff0000u);
-              float pk[GP];
-              if constexpr (GP >= 4) {
-#pragma unroll
-                for (int g4 = 0; g4 < GP; g4 += 4) {
-                  const float4 q4 = *reinterpret_cast<const float4*>(prow + k * GP + g4);
-                  pk[g4] = q4.x; pk[g4 + 1] = q4.y; pk[g4 + 2] = q4.z; pk[g4 + 3] = q4.w;
-                }
-              } else {
-#pragma unroll
-                for (int g = 0; g < GP; ++g) pk[g] = prow[k * GP + g];
-              }
-#pragma unroll
-              for (int g = 0; g < GP; ++g) {
-                acc[g][0] = fmaf(pk[g], v0, acc[g][0]);
-                acc[g][1] = fmaf(pk[g], v1, acc[g][1]);
-              }
-            }
-          }
-        }
-      }
-    }
-    __syncthreads();
-    // ---------------------------------------------------------------- V(c)
-    // Batched fetch of chunk c's surviving V tiles (BLASST §Kernel-ontwerp):
-    // the slots are free now that C(c-1) is done.
-    if (kPV && tid == 0 && c < nchunks && !*abort_flag) {
-      const int ns = ctl->n_surv[cb];
-      for (int s2 = 0; s2 < ns; ++s2) {
-        const int t = ctl->surv_tile[cb][s2];
-        const uint32_t bytes = static_cast<uint32_t>(tile_rows(t)) * D * 2;
-        ctl->surv_par[cb][s2] = nv_issued[s2] & 1u;
-        mbar_arrive_expect_tx(&ctl->v_full[s2], bytes);
-        bulk_load(sV + s2 * C::kTileBytes, vbase + static_cast<size_t>(j0 + t) * kTile * D, bytes,
-                  &ctl->v_full[s2]);
-        ++nv_issued[s2];
-      }
-    }
+  if (warp == kWarpS) {
+    tmem_alloc(&ctl->tmem_base, C::kTmemCols);
+    tmem_relinquish();
   }
-
-  // ------------------------------------------------------------------ output
-  if (kPV && !*abort_flag) {
-    if (warp < GP && lane == 0) {
-      sMl[warp * 2] = m_run;
-      sMl[warp * 2 + 1] = l_run;
+  if (warp < 4) {
+    // Q of the voting group as the score MMA's B operand: NQ rows x D,
+    // K-major, 128-byte swizzle (16-byte granule j of row g lands at
+    // j ^ (g & 7)); rows >= G are zero.  P slots: zero, so that their rows
+    // >= G stay zero for good.
+    for (int idx = tid; idx < NQ * (D / 8); idx += 128) {
+      const int g = idx / (D / 8), e8 = idx - (idx / (D / 8)) * (D / 8);
+      uint4 val = make_uint4(0u, 0u, 0u, 0u);
+      if (g < G)
+        val = *reinterpret_cast<const uint4*>(
+            p.q + (static_cast<size_t>(b) * p.Hq + kvh * G + g) * D + e8 * 8);
+      *reinterpret_cast<uint4*>(sQ + (e8 >> 3) * NQ * 128 + g * 128 + (((e8 & 7) ^ (g & 7)) << 4)) =
+          val;
     }
-    float* red = reinterpret_cast<float*>(sK);  // every K load has been consumed
-    const int dp = tid % C::kNDP, kg = tid / C::kNDP;
+    if (kPV)
+      for (int idx = tid; idx < NV * C::kPBytes / 16; idx += 128)
+        reinterpret_cast<uint4*>(sP)[idx] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+
+  if (warp >= 4) {
+    int n_v_issued = 0;
+    if (warp == kWarpK) {
+      // ---------------------------------------------------------- K producer
+      if (lane == 0) {
+        for (int t = NK; t < nt; ++t) {
+          if (!mbar_wait(&ctl->k_empty[t % NK], ((t / NK) & 1) ^ 1, abort_flag)) break;
+          issue_k(t);
+        }
+      }
+    } else if (warp == kWarpV) {
+      // ---------------------------------------------------------- V producer
+      if (kPV && lane == 0 && nt > 0) {
+        tma_prefetch_desc(&tmV);
+        for (int i = 0; i < nt; ++i) {
+          const int s = i % NV;
+          int t = i;
+          if (!kDenseV) {
+            if (!mbar_wait(&ctl->vq_full[s], (i / NV) & 1, abort_flag)) break;
+            t = *reinterpret_cast<volatile int*>(&ctl->kq[s]);
+            if (t < 0) break;
+          }
+          if (!mbar_wait(&ctl->slot_free[s], ((i / NV) & 1) ^ 1, abort_flag)) break;
+          mbar_arrive_expect_tx(&ctl->v_full[s], C::kTileBytes);
+#pragma unroll
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_3d(sV + s * C::kTileBytes + c * 16384, &tmV, &ctl->v_full[s], c * 64,
+                        (j0 + t) * kTile, bk);
+          n_v_issued = i + 1;
+        }
+      }
+    } else if (warp == kWarpS) {
+      // ---------------------------------------------------------- score MMAs
+      if (lane == 0 && nt > 0) {
+        constexpr uint32_t idS = idesc_bf16_f32(128, NQ, false, false);
+        const uint64_t dq = smem_desc(smem_u32(sQ), 16, 1024);
+        const uint32_t sKa = smem_u32(sK);
+        for (int t = 0; t < nt; ++t) {
+          const int st = t % NK, sb = t % NS;
+          if (!mbar_wait(&ctl->k_full[st], (t / NK) & 1, abort_flag)) break;
+          if (!mbar_wait(&ctl->s_empty[sb], ((t / NS) & 1) ^ 1, abort_flag)) break;
+          tc_fence_after();
+          const uint64_t dk = smem_desc(sKa + st * C::kTileBytes, 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t ka = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+            const uint32_t qa = ((kk >> 2) * NQ * 128 + (kk & 3) * 32) >> 4;
+            mma_bf16_ss(tmem + C::kColS + NQ * sb, dk + ka, dq + qa, idS, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&ctl->s_full[sb]);
+          mma_commit(&ctl->k_empty[st]);
+        }
+        mma_commit(&ctl->s_done);
+        mbar_wait(&ctl->s_done, 0, nullptr);  // all score MMAs done before TMEM is freed
+      }
+    } else {
+      // ---------------------------------------------------------- value MMAs
+      if (kPV && lane == 0 && nt > 0) {
+        constexpr uint32_t idO = idesc_bf16_f32(128, NQ, true, false);
+        const uint32_t sVa = smem_u32(sV), sPa = smem_u32(sP);
+        for (int i = 0;; ++i) {
+          const int s = i % NV;
+          if (!mbar_wait(&ctl->p_full[s], (i / NV) & 1, abort_flag)) break;
+          if (*reinterpret_cast<volatile int*>(&ctl->prec[s]) == 0) break;
+          if (!mbar_wait(&ctl->v_full[s], (i / NV) & 1, abort_flag)) break;
+          tc_fence_after();
+          const uint64_t dv = smem_desc(sVa + s * C::kTileBytes, 16384, 1024);
+          const uint64_t dp = smem_desc(sPa + s * C::kPBytes, 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < kTile / 16; ++kk) {
+            const uint32_t va = (kk * 2048) >> 4;
+            const uint32_t pa = ((kk >> 2) * NQ * 128 + (kk & 3) * 32) >> 4;
+            mma_bf16_ss(tmem + C::kColO + NQ * s, dv + va, dp + pa, idO, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(&ctl->slot_free[s]);
+        }
+        mma_commit(&ctl->pv_done);
+        mbar_wait(&ctl->pv_done, 0, nullptr);
+      }
+    }
+    if (lane == 0 && *abort_flag) {
+      // Let in-flight copies land before shared memory is released: the
+      // newest copy into stage s is the largest index < n with index % N == s.
+      // (With the test-only missing copy, stage 1 never received one.)
+      if (warp == kWarpK)
+        for (int s = 0; s < NK; ++s)
+          if (n_k_issued > s && !(p.fault_inject == 1 && s == 1))
+            mbar_wait(&ctl->k_full[s], ((s + ((n_k_issued - 1 - s) / NK) * NK) / NK) & 1, nullptr);
+      if (warp == kWarpV)
+        for (int s = 0; s < NV; ++s)
+          if (n_v_issued > s)
+            mbar_wait(&ctl->v_full[s], ((s + ((n_v_issued - 1 - s) / NV) * NV) / NV) & 1, nullptr);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ vote / softmax
+    const int key = tid;  // TMEM lane: key of the tile (scores), dimension (P.V)
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const float sl2 = p.scale_log2;
+    auto wwait = [&](uint64_t* bar, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
+    };
+    float m[GP], l[GP], acc[GP], macc[GP];
 #pragma unroll
     for (int g = 0; g < GP; ++g) {
-      red[(kg * GP + g) * D + 2 * dp] = acc[g][0];
-      red[(kg * GP + g) * D + 2 * dp + 1] = acc[g][1];
+      m[g] = -INFINITY;
+      l[g] = 0.f;
+      acc[g] = 0.f;
+      macc[g] = -INFINITY;
     }
-    __syncthreads();
-    for (int idx = tid; idx < G * D; idx += kDecThreads) {
-      const int g = idx / D, e = idx - (idx / D) * D;
-      float sum = 0.f;
+    uint32_t skipped = 0;
+    int kept = 0;
+    bool ok = true;
+
+    // Fold the P.V result of kept tile j (slot j % NV) into acc.
+    auto accumulate = [&](int j) {
+      float o[GP];
+      tmem_ld_cols<GP>(lane_base + C::kColO + NQ * (j % NV), o);
+      tmem_wait_ld();
+      const float* ms = sMs + (j % (2 * NV)) * GP;
 #pragma unroll
-      for (int kg2 = 0; kg2 < C::kNKG; ++kg2) sum += red[(kg2 * GP + g) * D + e];
-      const size_t row = static_cast<size_t>(b) * p.Hq + kvh * G + g;
-      if (p.S == 1) {
-        const float l = sMl[g * 2 + 1];
-        p.o[row * D + e] = __float2bfloat16_rn(l > 0.f ? sum / l : 0.f);
-      } else {
-        float* pr = p.part + (row * p.S + split) * (D + 2);
-        pr[e] = sum;
-        if (e == 0) {
-          const float m = sMl[g * 2];
-          pr[D] = (m == -INFINITY) ? -INFINITY : m * sl2;
-          pr[D + 1] = sMl[g * 2 + 1];
+      for (int g = 0; g < GP; ++g) {
+        const float mj = ms[g];
+        const float f = (macc[g] == -INFINITY) ? 0.f : ex2_approx((macc[g] - mj) * sl2);
+        acc[g] = fmaf(acc[g], f, o[g]);
+        macc[g] = mj;
+      }
+    };
+
+    for (int t = 0; t < nt; ++t) {
+      const int sb = t % NS;
+      const bool got = wwait(&ctl->s_full[sb], (t / NS) & 1);
+      ok = ok && got;
+      tc_fence_after();
+      float s[GP];
+      if (got) {
+        tmem_ld_cols<GP>(lane_base + C::kColS + NQ * sb, s);
+        tmem_wait_ld();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->s_empty[sb]);
+      const bool valid_key = got && key < tile_rows(t);
+#pragma unroll
+      for (int g = 0; g < GP; ++g)
+        if (!valid_key) s[g] = -INFINITY;
+
+      // Tile maximum of each row: warp maxima, exchanged through shared
+      // memory at one 128-thread barrier per tile (double-buffered by tile
+      // parity, so a warp that runs ahead cannot overwrite unread values).
+      float mine = -INFINITY;
+#pragma unroll
+      for (int g = 0; g < GP; ++g) {
+        const float wm = warp_max(s[g]);
+        if (lane == g) mine = wm;
+      }
+      if (lane < GP) sRed[((t & 1) * GP + lane) * 4 + warp] = mine;
+      named_bar_sync(1, 128);
+      float tm[GP];
+#pragma unroll
+      for (int g = 0; g < GP; ++g) {
+        const float4 r = *reinterpret_cast<const float4*>(sRed + ((t & 1) * GP + g) * 4);
+        tm[g] = fmaxf(fmaxf(r.x, r.y), fmaxf(r.z, r.w));
+      }
+
+      // Vote: skip iff every row r has tile_max_r - m_r < ln(lambda)/scale.
+      float cval = -INFINITY;
+#pragma unroll
+      for (int g = 0; g < GP; ++g)
+        if (g < G && tm[g] != -INFINITY)
+          cval = fmaxf(cval, (m[g] == -INFINITY) ? INFINITY : tm[g] - m[g]);
+      const bool skip = kVote && cval < p.thr_raw;
+      if (tid == 0) {
+        const long gi = static_cast<long>(bk) * p.nT + j0 + t;
+        if (p.mask != nullptr) p.mask[gi] = skip ? 1 : 0;
+        if (p.margin != nullptr) p.margin[gi] = (cval == INFINITY) ? INFINITY : cval * p.scale;
+        skipped += skip ? 1u : 0u;
+      }
+      if (skip) continue;  // skipped tiles never raise m (lambda <= 1)
+
+      float mn[GP];
+#pragma unroll
+      for (int g = 0; g < GP; ++g) mn[g] = fmaxf(m[g], tm[g]);
+      if (kPV) {
+        const int sl = kept % NV;
+        // The slot's previous tile (kept - NV) must be through its P.V MMA
+        // before its V, P and O space is reused.
+        if (kept >= NV) ok = wwait(&ctl->slot_free[sl], ((kept / NV) - 1) & 1) && ok;
+        if (!kDenseV && tid == 0) {
+          ctl->kq[sl] = t;
+          mbar_arrive(&ctl->vq_full[sl]);
+        }
+        if (kept >= NV) {
+          tc_fence_after();
+          accumulate(kept - NV);
+        }
+        // P for this tile as the value MMA's B operand: NQ rows x 128 keys,
+        // K-major, 128-byte swizzle; this thread writes column `key`.
+        uint8_t* ps = sP + sl * C::kPBytes + (key >> 6) * NQ * 128 + (key & 7) * 2;
+        const int j8 = (key & 63) >> 3;
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
+          const float alpha = (m[g] == -INFINITY) ? 0.f : ex2_approx((m[g] - mn[g]) * sl2);
+          const float mb = (mn[g] == -INFINITY) ? 0.f : mn[g] * sl2;
+          const float pv = ex2_approx(fmaf(s[g], sl2, -mb));
+          l[g] = fmaf(l[g], alpha, pv);
+          if (g < G)
+            *reinterpret_cast<__nv_bfloat16*>(ps + g * 128 + ((j8 ^ (g & 7)) << 4)) =
+                __float2bfloat16_rn(pv);
+        }
+        float mine_m = 0.f;
+#pragma unroll
+        for (int g = 0; g < GP; ++g)
+          if (tid == g) mine_m = mn[g];
+        if (tid < GP) sMs[(kept % (2 * NV)) * GP + tid] = mine_m;
+        if (tid == 0) ctl->prec[sl] = 1;
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->p_full[sl]);
+        ++kept;
+      }
+#pragma unroll
+      for (int g = 0; g < GP; ++g) m[g] = mn[g];
+    }
+
+    if (kPV) {
+      // End of the kept stream for the V producer and the value-MMA issuer.
+      const int sl = kept % NV;
+      if (kept >= NV) ok = wwait(&ctl->slot_free[sl], ((kept / NV) - 1) & 1) && ok;
+      if (tid == 0) {
+        if (!kDenseV) {
+          ctl->kq[sl] = -1;
+          mbar_arrive(&ctl->vq_full[sl]);
+        }
+        ctl->prec[sl] = 0;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->p_full[sl]);
+      named_bar_sync(1, 128);  // the last tile's maxima (sMs) are visible
+      for (int j = max(0, kept - NV); j < kept; ++j) {
+        ok = wwait(&ctl->slot_free[j % NV], (j / NV) & 1) && ok;
+        tc_fence_after();
+        accumulate(j);
+      }
+      // Row sums: per-key partials over the 128 threads.
+#pragma unroll
+      for (int g = 0; g < GP; ++g) {
+        float v = l[g];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) sLRed[g * 4 + warp] = v;
+      }
+      named_bar_sync(1, 128);
+      if (ok && !*abort_flag && key < D) {
+        const int e = key;
+#pragma unroll
+        for (int g = 0; g < GP; ++g) {
+          if (g >= G) break;
+          const float4 r = *reinterpret_cast<const float4*>(sLRed + g * 4);
+          const float lt = (r.x + r.y) + (r.z + r.w);
+          const size_t row = static_cast<size_t>(b) * p.Hq + kvh * G + g;
+          if (p.S == 1) {
+            p.o[row * D + e] = __float2bfloat16_rn(lt > 0.f ? acc[g] / lt : 0.f);
+          } else {
+            float* pr = p.part + (row * p.S + split) * (D + 2);
+            pr[e] = acc[g];
+            if (e == 0) {
+              pr[D] = (m[g] == -INFINITY) ? -INFINITY : m[g] * sl2;
+              pr[D + 1] = lt;
+            }
+          }
         }
       }
     }
+    if (tid == 0 && p.counts != nullptr) p.counts[static_cast<long>(bk) * p.S + split] = skipped;
+    tc_fence_before();
+    __syncwarp();
   }
-  if (warp == C::kVoteWarp && lane == 0 && p.counts != nullptr)
-    p.counts[static_cast<long>(bk) * p.S + split] = skipped;
-  if (tid == 0) {
-    if (*abort_flag) {
-      // Let in-flight copies land before shared memory is released.
-#pragma unroll
-      for (int s2 = 0; s2 < kKStages; ++s2)
-        if (k_last[s2] >= 0) mbar_wait(&ctl->k_full[s2], (k_last[s2] / kKStages) & 1, nullptr);
-      for (int s = 0; s < 2; ++s)
-        if (nv_issued[s] > 0) mbar_wait(&ctl->v_full[s], (nv_issued[s] - 1) & 1, nullptr);
-      report_timeout(p.status);
-    }
+
+  // ------------------------------------------------------------------ teardown
+  barrier_sync(2, kDecThreads);
+  if (warp == kWarpS) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
   }
+  if (tid == 0 && *abort_flag) report_timeout(p.status);
 }
 
 // Log-sum-exp merge of the per-split partial states: one warp per (b, h_q).
@@ -506,13 +545,14 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const float* __restri
 }
 
 template <int D, int GP, Mode MODE>
-cudaError_t launch_dec(const DecodeParams& p, cudaStream_t st) {
-  using C = DecodeCfg<D, GP>;
+cudaError_t launch_dec(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
+                       cudaStream_t st) {
+  using C = DecCfg<D, GP>;
   auto* fn = decode_kernel<D, GP, MODE>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const long ctas = static_cast<long>(p.B) * p.Hkv * p.S;
-  fn<<<dim3(static_cast<unsigned>(ctas)), dim3(C::kThreads), C::kSmemBytes, st>>>(p);
+  fn<<<dim3(static_cast<unsigned>(ctas)), dim3(kDecThreads), C::kSmemBytes, st>>>(tk, tv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess || MODE == Mode::kCount || p.S == 1) return e;
   const int rows = p.B * p.Hq;
@@ -521,26 +561,31 @@ cudaError_t launch_dec(const DecodeParams& p, cudaStream_t st) {
 }
 
 template <int D, int GP>
-cudaError_t launch_dec_mode(const DecodeParams& p, Mode mode, cudaStream_t st) {
+cudaError_t launch_dec_mode(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
+                            Mode mode, cudaStream_t st) {
   switch (mode) {
-    case Mode::kDense: return launch_dec<D, GP, Mode::kDense>(p, st);
-    case Mode::kSparse: return launch_dec<D, GP, Mode::kSparse>(p, st);
-    default: return launch_dec<D, GP, Mode::kCount>(p, st);
+    case Mode::kDense: return launch_dec<D, GP, Mode::kDense>(tk, tv, p, st);
+    case Mode::kSparse: return launch_dec<D, GP, Mode::kSparse>(tk, tv, p, st);
+    default: return launch_dec<D, GP, Mode::kCount>(tk, tv, p, st);
   }
 }
 
 template <int D>
-cudaError_t launch_dec_g(const DecodeParams& p, Mode mode, cudaStream_t st) {
-  if (p.G <= 1) return launch_dec_mode<D, 1>(p, mode, st);
-  if (p.G <= 2) return launch_dec_mode<D, 2>(p, mode, st);
-  if (p.G <= 4) return launch_dec_mode<D, 4>(p, mode, st);
-  return launch_dec_mode<D, 8>(p, mode, st);
+cudaError_t launch_dec_g(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
+                         Mode mode, cudaStream_t st) {
+  if (p.G <= 1) return launch_dec_mode<D, 1>(tk, tv, p, mode, st);
+  if (p.G <= 2) return launch_dec_mode<D, 2>(tk, tv, p, mode, st);
+  if (p.G <= 4) return launch_dec_mode<D, 4>(tk, tv, p, mode, st);
+  if (p.G <= 8) return launch_dec_mode<D, 8>(tk, tv, p, mode, st);
+  return launch_dec_mode<D, 16>(tk, tv, p, mode, st);
 }
 
 }  // namespace
 
-cudaError_t launch_decode(const DecodeParams& p, Mode mode, cudaStream_t st) {
-  return (p.d == 128) ? launch_dec_g<128>(p, mode, st) : launch_dec_g<64>(p, mode, st);
+cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
+                          Mode mode, cudaStream_t st) {
+  return (p.d == 128) ? launch_dec_g<128>(tk, tv, p, mode, st)
+                      : launch_dec_g<64>(tk, tv, p, mode, st);
 }
 
 }  // namespace ssattn

@@ -153,7 +153,7 @@ ss_status decode_impl(const void* q, const void* k, const void* v, void* o, int 
   if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Lk < 1 || S < 1 || !scale_ok(scale))
     return SS_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return SS_ERR_UNSUPPORTED;
-  if (Hq / Hkv > 8) return SS_ERR_UNSUPPORTED;  // voting group held in registers
+  if (Hq / Hkv > 16) return SS_ERR_UNSUPPORTED;  // voting group = MMA N of at most 16 rows
   const long nT = ceil_div(Lk, kTile);
   const long ctas = static_cast<long>(B) * Hkv * S;
   if (ctas > 0x7fffffffL) return SS_ERR_INVALID_ARG;
@@ -162,6 +162,10 @@ ss_status decode_impl(const void* q, const void* k, const void* v, void* o, int 
   }
   ss_status st = check_device();
   if (st != SS_OK) return st;
+  CUtensorMap tk, tv;
+  if (!make_map(&tk, k, d, Lk, static_cast<long>(B) * Hkv) ||
+      !make_map(&tv, v, d, Lk, static_cast<long>(B) * Hkv))
+    return SS_ERR_CUDA;
 
   DecodeParams p{};
   p.B = B;
@@ -177,8 +181,6 @@ ss_status decode_impl(const void* q, const void* k, const void* v, void* o, int 
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.thr_raw = thr_raw;
   p.q = static_cast<const __nv_bfloat16*>(q);
-  p.k = static_cast<const __nv_bfloat16*>(k);
-  p.v = static_cast<const __nv_bfloat16*>(v);
   p.o = static_cast<__nv_bfloat16*>(o);
   p.part = static_cast<float*>(ws);
   p.counts = counts;
@@ -188,7 +190,7 @@ ss_status decode_impl(const void* q, const void* k, const void* v, void* o, int 
   p.count_only = count_only ? 1 : 0;
   p.fault_inject = dbg ? dbg->fault_inject : 0;
   const Mode mode = count_only ? Mode::kCount : (dense ? Mode::kDense : Mode::kSparse);
-  cudaError_t e = launch_decode(p, mode, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_decode(tk, tv, p, mode, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 

@@ -60,7 +60,8 @@ extern "C" {
 typedef enum {
   SS_OK = 0,
   SS_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad shape, lambda or scale */
-  SS_ERR_UNSUPPORTED = 2,  /* d not in {64,128}, or the current device is not sm_103 */
+  SS_ERR_UNSUPPORTED = 2,  /* d not in {64,128}, decode with Hq/Hkv > 16, or the current
+                              device is not sm_103 */
   SS_ERR_CUDA = 3,         /* a CUDA runtime call failed (launch, copy, sync) */
   SS_ERR_TIMEOUT = 4,      /* a kernel's bounded wait expired (logic error; reported, not hung) */
   SS_ERR_WORKSPACE = 5     /* decode workspace missing or too small */

@@ -91,7 +91,7 @@ def test_prefill_rejects_before_launch(capi, kw, expect):
 @pytest.mark.parametrize("kw,expect", [
     (dict(S=0), "SS_ERR_INVALID_ARG"),
     (dict(Lk=0), "SS_ERR_INVALID_ARG"),
-    (dict(Hq=32, Hkv=2), "SS_ERR_UNSUPPORTED"),       # vote group > 8
+    (dict(Hq=64, Hkv=2), "SS_ERR_UNSUPPORTED"),       # vote group > 16
     (dict(S=4, ws=None), "SS_ERR_WORKSPACE"),
     (dict(S=4, ws_bytes=16), "SS_ERR_WORKSPACE"),
 ])

@@ -29,6 +29,8 @@ SHAPES = [
     (1, 4, 1, 100, 128, 1),     # one partial tile
     (1, 4, 1, 300, 128, 8),     # more splits than tiles: empty splits
     (2, 8, 1, 900, 64, 3),      # d = 64 with an 8-row vote group
+    (1, 16, 1, 1000, 128, 2),   # G = 16 (the largest vote group)
+    (2, 24, 2, 700, 64, 1),     # G = 12 (padded to 16 rows)
 ]
 
 
