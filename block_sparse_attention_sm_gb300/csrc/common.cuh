@@ -11,6 +11,7 @@
 namespace ssattn {
 
 constexpr int kTile = 128;  // key tile and prefill query block
+constexpr int kVoteChunkTiles = 2048;  // prefill: key tiles decided per vote/compute run
 
 // Device status word: kernels that give up a bounded wait OR a code into the
 // word whose address the launch passes them (module memory of the C-ABI
@@ -40,6 +41,7 @@ struct PrefillParams {
   int G;          // Hq / Hkv
   int nQB, nT;    // query blocks, key tiles
   int causal;
+  int chunk_tiles;   // key tiles decided per vote/compute run (<= the kernel's capacity)
   float scale_log2;  // scale * log2(e): exponent factor on raw scores
   float scale;       // natural-log factor (for margins)
   float thr_raw;     // ln(lambda) / scale: skip iff tile_max - m < thr_raw (raw units)

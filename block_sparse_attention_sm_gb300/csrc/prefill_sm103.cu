@@ -7,29 +7,46 @@
 // exp(scale*(tile_max - m)) < lambda, the tile's exponentials and its P.V MMA
 // are skipped and it adds nothing to l or O.
 //
+// Decisions first, values second.  With lambda <= 1 a skipped tile never
+// raises a row's maximum, so the maximum m_r before tile j is the prefix
+// maximum of the row's scores over tiles < j whatever was skipped, and every
+// decision depends on the scores alone.  Each CTA therefore runs
+//   a vote pass:    S_j for every tile into double-buffered TMEM, row maxima,
+//                   the vote against the exact running maximum; no
+//                   exponentials, so the score MMAs stream back to back;
+//   a compute pass: over the kept tiles only, S_j again, P = exp2((S - m) *
+//                   scale * log2e) with m the row's final maximum from the
+//                   vote pass (so O never needs a rescale), O += P V_j.
+// The kept set, the counters and O equal those of the one-pass definition;
+// kept tiles pay their QK^T twice, skipped tiles once.  Very long keys are
+// handled in runs of p.chunk_tiles (at most 2048) tiles: vote pass, then
+// compute pass, per run, with O rescaled once when a later run raises a row
+// maximum.  The dense path (lambda = 0) has no vote pass: one online pass
+// with a lazily rescaled maximum.
+//
 // One CTA = two 128-row query blocks (t = 0, 1) of one (b, h_q), sharing every
 // K/V tile; 384 threads (3 warpgroups; registers re-split with setmaxnreg):
 //   warps 0-3 / 4-7  softmax of query block 0 / 1: thread = query row = TMEM
-//                    lane.  It loads its 128 scores from TMEM once, takes the
-//                    row maximum, votes (a bar.red.and over the block's 128
-//                    threads) and, for kept tiles, writes P as bf16 over the
-//                    first 64 columns of S; lazy O rescale; epilogue O / l.
-//   warp 8           TMA producer: both Q blocks, then the K ring.
-//   warp 9           TMA producer: the V ring.
-//   warp 10          TMEM allocator + single-thread tcgen05 MMA issuer, in the
-//                    order ... PV_0(i-1), S_0(i), PV_1(i-1), S_1(i) ... so one
+//                    lane.  Vote pass: loads the row's 128 scores, row
+//                    maximum, vote (a bar.red.and over the block's 128
+//                    threads).  Compute pass: writes P as bf16 over the first
+//                    64 columns of S; epilogue O / l.
+//   warp 8           TMA producer: both Q blocks, then one FIFO ring of
+//                    tiles: K of every tile (vote pass), then K and V of the
+//                    kept tiles (compute pass).
+//   warp 10          TMEM allocator + single-thread tcgen05 MMA issuer.  Vote
+//                    pass: S_0(i), S_1(i) into score buffer i % 2, one
+//                    commit for both.
+//                    Compute pass, over the tiles kept by either block:
+//                    ... PV_0(prev), S_0(u), PV_1(prev), S_1(u) ... so one
 //                    block's softmax overlaps the other block's MMAs.
 //                    S_t = Q_t K^T: SS form, both operands K-major, 128-byte
 //                    swizzle.  O_t += P_t V: TS form, P_t from TMEM, V MN-major.
-// TMEM (512 columns): S_0 [0,128), S_1 [128,256) (P_t in the first 64 columns
-// of S_t), O_0 [256, 256+d), O_1 [384, 384+d).  tcgen05 MMAs of a CTA execute
-// in issue order, so S_t(i+1) (issued after PV_t(i)) cannot overwrite P_t(i)
-// early, and the commit after S_t(i+1) also covers PV_t(i).
-//
-// Exactness of the decisions: the vote uses the true running maximum
-// (max over every earlier tile).  The exponentials use m_used, which only
-// follows it when it has grown by more than 2^8 in the exp2 domain (then O and
-// l are rescaled); O / l is the same either way.
+// TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256, 256+d),
+// O_1 [384, 384+d); the vote pass's second score buffers of the first chunk
+// are O_0 / O_1 (the compute pass's first P.V overwrites them).  tcgen05 MMAs
+// of a CTA execute in issue order, so an MMA issued after PV_t cannot
+// overwrite P_t early, and a commit covers every MMA issued before it.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -39,45 +56,70 @@ namespace ssattn {
 
 namespace {
 
-constexpr float kRescaleLog2 = 8.0f;  // lazy-rescale slack, exp2 domain
+constexpr float kRescaleLog2 = 8.0f;  // lazy-rescale slack of the dense path, exp2 domain
 constexpr int kThreads = 384;         // three warpgroups
-constexpr int kWarpK = 8, kWarpV = 9, kWarpMma = 10;  // warp 11 idles
+constexpr int kWarpLoad = 8, kWarpMma = 10;  // warp 11 idles
+constexpr int kWarpMma2 = 9;  // second score issuer of the vote pass
 // Register split: launched at 168 per thread (384 x 168 = 64512); the
-// producer/MMA warpgroup drops to 56 and the two softmax warpgroups rise to
-// 224: 128 x 56 + 256 x 224 = 64512, i.e. exactly the launch pool.
-constexpr int kLaunchRegs = 168, kRegsIssue = 56, kRegsSoftmax = 224;
-static_assert(128 * kRegsIssue + 256 * kRegsSoftmax == kThreads * kLaunchRegs,
+// producer/MMA warpgroup drops to kRegsIssue and the two softmax warpgroups
+// rise to kRegsSoftmax, with 128 x issue + 256 x softmax = 64512, i.e.
+// exactly the launch pool.  The voting kernels' issuer walks the kept-tile
+// masks and needs more than the dense kernel's.
+constexpr int kLaunchRegs = 168;
+template <Mode MODE>
+constexpr int kRegsIssue = (MODE == Mode::kDense) ? 72 : 104;
+template <Mode MODE>
+constexpr int kRegsSoftmax = (kThreads * kLaunchRegs - 128 * kRegsIssue<MODE>) / 256;
+static_assert(128 * kRegsIssue<Mode::kDense> + 256 * kRegsSoftmax<Mode::kDense> ==
+                  kThreads * kLaunchRegs &&
+              128 * kRegsIssue<Mode::kSparse> + 256 * kRegsSoftmax<Mode::kSparse> ==
+                  kThreads * kLaunchRegs,
               "register split must equal the launch pool");
+static_assert(kRegsSoftmax<Mode::kDense> % 8 == 0 && kRegsSoftmax<Mode::kSparse> % 8 == 0,
+              "setmaxnreg takes multiples of 8");
+constexpr int kMaskWords = kVoteChunkTiles / 32;  // mask capacity of one chunk
 
 template <int D>
 struct PrefillCfg {
   static constexpr int kChunks = D / 64;            // 128-byte swizzle chunks per row
   static constexpr int kTileBytes = kTile * D * 2;  // one 128 x D bf16 tile
-  static constexpr int kKStages = (D == 128) ? 3 : 4;
-  static constexpr int kVStages = (D == 128) ? 2 : 4;
+  // One FIFO ring of tile slots for K and V: the vote pass streams K tiles
+  // through every slot; the compute pass loads K(u), V(u), K(u'), V(u'), ...
+  // and frees them in the same order (an MMA that reads V(u) is issued
+  // before the one that reads K(u'), and MMAs complete in issue order).
+  static constexpr int kRingSlots = (D == 128) ? 5 : 12;
   static constexpr int kQOff = 0;  // two query blocks
-  static constexpr int kKOff = kQOff + 2 * kTileBytes;
-  static constexpr int kVOff = kKOff + kKStages * kTileBytes;
-  static constexpr int kCtlOff = kVOff + kVStages * kTileBytes;
-  static constexpr int kCtlBytes = 1024;
+  static constexpr int kRingOff = kQOff + 2 * kTileBytes;
+  static constexpr int kCtlOff = kRingOff + kRingSlots * kTileBytes;
+  static constexpr int kCtlBytes = 2048;
   static constexpr int kSmemBytes = kCtlOff + kCtlBytes + 1024;  // + alignment slack
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
   static constexpr uint32_t kColS = 0;    // S_t at kColS + 128 t
   static constexpr uint32_t kColO = 256;  // O_t at kColO + 128 t
   static constexpr uint32_t kTmemCols = 512;
 };
 
-template <int NK, int NV>
+template <int NR>
 struct PrefillCtl {
   uint64_t q_full;
-  uint64_t k_full[NK], k_empty[NK];
-  uint64_t v_full[NV], v_empty[NV];
-  uint64_t s_full[2], p_full[2];
+  uint64_t r_full[NR], r_empty[NR];        // tile ring
+  // Vote pass, per score buffer b (both blocks' S in it): one commit after
+  // S_0 and S_1, and one release by the 8 softmax warps (the issuer stands in
+  // for a block that has no tile there), so the issuer pays one wait and one
+  // commit per tile pair.
+  uint64_t s1_full[2], s1_empty[2];
+  uint64_t s_full[2], p_full[2];           // compute pass: [block]
+  // Per chunk parity: the 8 softmax warps are done voting.  Two barriers, so
+  // that a reader one chunk behind (the V producer, when a chunk keeps no
+  // tile) never sees a phase two chunks ahead.
+  uint64_t votes_done[2];
+  uint64_t mask_free[2];                   // per chunk parity: its 2 readers are done
   uint64_t o_done;
-  uint64_t mma_done;
+  uint64_t mma_done, mma_done2;
   uint32_t tmem_base;
   int abort_flag;
-  int dec[2];
   float red[2][2][4];
+  uint32_t kmask[2][2][kMaskWords];  // kept tiles: [chunk parity][block][bit]
 };
 
 template <int D, Mode MODE>
@@ -85,18 +127,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
   using C = PrefillCfg<D>;
-  constexpr int NK = C::kKStages, NV = C::kVStages;
+  constexpr int NR = C::kRingSlots;
   constexpr bool kPV = (MODE != Mode::kCount);
   constexpr bool kVote = (MODE != Mode::kDense);
-  using Ctl = PrefillCtl<NK, NV>;
+  using Ctl = PrefillCtl<NR>;
   static_assert(sizeof(Ctl) <= C::kCtlBytes, "control block overflow");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sQ = smem + C::kQOff;
-  uint8_t* sK = smem + C::kKOff;
-  uint8_t* sV = smem + C::kVOff;
+  uint8_t* sR = smem + C::kRingOff;
   auto* ctl = reinterpret_cast<Ctl*>(smem + C::kCtlOff);
   volatile int* abort_flag = &ctl->abort_flag;
 
@@ -124,22 +165,59 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int nmax = max(n_t[0], n_t[1]);
 
+  // Vote pass whenever decisions are wanted (the dense instantiation is
+  // launched only without debug outputs); the kept-tile masks are needed
+  // only when a compute pass follows.
+  constexpr bool vote_pass = kVote;
+  constexpr bool use_masks = vote_pass && kPV;
+  const int nchunks = vote_pass ? (nmax + p.chunk_tiles - 1) / p.chunk_tiles : (nmax > 0 ? 1 : 0);
+  auto chunk_begin = [&](int c) { return vote_pass ? c * p.chunk_tiles : 0; };
+  auto chunk_end = [&](int c) { return vote_pass ? min(nmax, (c + 1) * p.chunk_tiles) : nmax; };
+  auto mask_word = [&](int c, int t, int w) -> uint32_t {
+    return *reinterpret_cast<volatile uint32_t*>(&ctl->kmask[c & 1][t][w]);
+  };
+  // Is tile u (in chunk c) computed for block t?
+  auto kept = [&](int c, int t, int u) -> bool {
+    if (!use_masks) return u < n_t[t];
+    const int r = u - c * p.chunk_tiles;
+    return ((mask_word(c, t, r >> 5) >> (r & 31)) & 1u) != 0;
+  };
+  // First tile >= from in chunk c that block `which` (0, 1; 2 = either)
+  // computes; the chunk end if none.
+  auto next_kept = [&](int c, int which, int from) -> int {
+    const int e = chunk_end(c);
+    if (!use_masks) return (which == 2) ? from : (from < n_t[which] ? from : e);
+    int u = from;
+    while (u < e) {
+      const int r = u - c * p.chunk_tiles;
+      const int w = r >> 5;
+      uint32_t bits = (which == 2) ? (mask_word(c, 0, w) | mask_word(c, 1, w)) : mask_word(c, which, w);
+      bits >>= (r & 31);
+      if (bits != 0u) return min(e, u + __ffs(bits) - 1);
+      u += 32 - (r & 31);
+    }
+    return e;
+  };
+
   if (tid == 0) {
     mbar_init(&ctl->q_full, 1);
-    for (int s = 0; s < NK; ++s) {
-      mbar_init(&ctl->k_full[s], 1);
-      mbar_init(&ctl->k_empty[s], 1);
-    }
-    for (int s = 0; s < NV; ++s) {
-      mbar_init(&ctl->v_full[s], 1);
-      mbar_init(&ctl->v_empty[s], 1);
+    for (int s = 0; s < NR; ++s) {
+      mbar_init(&ctl->r_full[s], 1);
+      mbar_init(&ctl->r_empty[s], 1);
     }
     for (int t = 0; t < 2; ++t) {
+      mbar_init(&ctl->s1_full[t], 1);
+      mbar_init(&ctl->s1_empty[t], 8);
       mbar_init(&ctl->s_full[t], 1);
       mbar_init(&ctl->p_full[t], 128);
     }
+    mbar_init(&ctl->votes_done[0], 8);
+    mbar_init(&ctl->votes_done[1], 8);
+    mbar_init(&ctl->mask_free[0], 2);
+    mbar_init(&ctl->mask_free[1], 2);
     mbar_init(&ctl->o_done, 1);
     mbar_init(&ctl->mma_done, 1);
+    mbar_init(&ctl->mma_done2, 1);
     ctl->abort_flag = 0;
     fence_mbar_init();
   }
@@ -156,13 +234,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Each warpgroup's code below runs to the end of the kernel under its own
   // register budget; the two paths meet only at the final named barrier.
   if (warp >= 8) {
-  setmaxnreg_dec<kRegsIssue>();
-  int n_k_issued = 0, n_v_issued = 0;  // producer bookkeeping for teardown
-  if (warp == kWarpK) {
-    // ---------------------------------------------------------- Q + K producer
+  constexpr uint32_t kRegsDown = kRegsIssue<MODE>;
+  setmaxnreg_dec<kRegsDown>();
+  int n_issued = 0;  // producer bookkeeping for teardown: ring entries issued
+  if (warp == kWarpLoad) {
+    // ---------------------------------------------------------- TMA producer
     if (lane == 0 && nmax > 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
+      if (kPV) tma_prefetch_desc(&tmV);
       const int nq = (rows[0] > 0 ? 1 : 0) + (rows[1] > 0 ? 1 : 0);
       mbar_arrive_expect_tx(&ctl->q_full, nq * C::kTileBytes);
 #pragma unroll
@@ -171,84 +251,128 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_3d(sQ + t * C::kTileBytes + c * 16384, &tmQ, &ctl->q_full, c * 64, r0[t], bh);
-      for (int i = 0; i < nmax; ++i) {
-        const int st = i % NK;
-        if (!mbar_wait(&ctl->k_empty[st], ((i / NK) & 1) ^ 1, abort_flag)) break;
-        mbar_arrive_expect_tx(&ctl->k_full[st], C::kTileBytes);
+      // Next ring entry: tile u of K or V.
+      auto load_tile = [&](const CUtensorMap* map, int u) -> bool {
+        const int st = n_issued % NR;
+        if (!mbar_wait(&ctl->r_empty[st], ((n_issued / NR) & 1) ^ 1, abort_flag)) return false;
+        mbar_arrive_expect_tx(&ctl->r_full[st], C::kTileBytes);
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(sK + st * C::kTileBytes + c * 16384, &tmK, &ctl->k_full[st], c * 64,
-                      i * kTile, zk);
-        n_k_issued = i + 1;
+          tma_load_3d(sR + st * C::kTileBytes + c * 16384, map, &ctl->r_full[st], c * 64,
+                      u * kTile, zk);
+        ++n_issued;
+        return true;
+      };
+      bool ok = true;
+      for (int c = 0; ok && c < nchunks; ++c) {
+        if (vote_pass) {
+          for (int u = chunk_begin(c); ok && u < chunk_end(c); ++u) ok = load_tile(&tmK, u);
+          if (!kPV) continue;
+          ok = ok && mbar_wait(&ctl->votes_done[c & 1], (c >> 1) & 1, abort_flag);
+        }
+        for (int u = next_kept(c, 2, chunk_begin(c)); ok && u < chunk_end(c); u = next_kept(c, 2, u + 1))
+          ok = load_tile(&tmK, u) && load_tile(&tmV, u);
+        if (use_masks) mbar_arrive(&ctl->mask_free[c & 1]);
       }
     }
-  } else if (warp == kWarpV) {
-    // ---------------------------------------------------------- V producer
-    if (kPV && lane == 0 && nmax > 0) {
-      tma_prefetch_desc(&tmV);
-      for (int i = 0; i < nmax; ++i) {
-        const int st = i % NV;
-        if (!mbar_wait(&ctl->v_empty[st], ((i / NV) & 1) ^ 1, abort_flag)) break;
-        mbar_arrive_expect_tx(&ctl->v_full[st], C::kTileBytes);
-#pragma unroll
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(sV + st * C::kTileBytes + c * 16384, &tmV, &ctl->v_full[st], c * 64,
-                      i * kTile, zk);
-        n_v_issued = i + 1;
-      }
-    }
-  } else if (warp == kWarpMma) {
-    // ---------------------------------------------------------- MMA issuer
+  } else if (warp == kWarpMma || warp == kWarpMma2) {
+    // ---------------------------------------------------------- MMA issuers
+    // Issuing blocks until the tensor pipe takes each MMA, so the pipe idles
+    // while its issuer waits or commits.  In the first chunk's vote pass two
+    // threads issue the score MMAs -- even tiles into score buffer 0 (warp
+    // 10), odd tiles into buffer 1 (warp 9) -- so one keeps the pipe fed
+    // while the other synchronises.  Warp 10 issues everything else.
     if (lane == 0 && nmax > 0) {
       constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idO = idesc_bf16_f32(128, D, false, true);
-      const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
+      const uint32_t sQa = smem_u32(sQ), sRa = smem_u32(sR);
       // Descriptors are built once per operand tile and advanced by adding the
       // encoded (>>4) byte offset to the start-address field; shared-memory
       // offsets here stay far below the field's 2^18-byte range, so the add
       // never carries out of it.
-      auto issue_s = [&](int t, int kst) {
+      auto issue_s = [&](int t, int kst, uint32_t col) {
         const uint64_t dq = smem_desc(sQa + t * C::kTileBytes, 16, 1024);
-        const uint64_t dk = smem_desc(sKa + kst * C::kTileBytes, 16, 1024);
+        const uint64_t dk = smem_desc(sRa + kst * C::kTileBytes, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-          mma_bf16_ss(tmem + C::kColS + 128 * t, dq + koff, dk + koff, idS, kk > 0 ? 1u : 0u);
+          mma_bf16_ss(tmem + col, dq + koff, dk + koff, idS, kk > 0 ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int t, int vst, uint32_t acc) {
-        const uint64_t dv = smem_desc(sVa + vst * C::kTileBytes, 16384, 1024);
+        const uint64_t dv = smem_desc(sRa + vst * C::kTileBytes, 16384, 1024);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk)
           mma_bf16_ts(tmem + C::kColO + 128 * t, tmem + C::kColS + 128 * t + kk * 8,
                       dv + ((kk * 2048) >> 4), idO, (acc | kk) ? 1u : 0u);
       };
-      bool ok = mbar_wait(&ctl->q_full, 0, abort_flag) && mbar_wait(&ctl->k_full[0], 0, abort_flag);
-      uint32_t o_acc[2] = {0u, 0u};
-      if (ok) {
+      bool ok = mbar_wait(&ctl->q_full, 0, abort_flag);
+      // One vote-pass tile: ring entry `e`, score buffer `bsel`, `n` earlier uses of it.
+      auto vote_tile = [&](int u, int e, int bsel, int n) -> bool {
+        const int kst = e % NR;
+        if (!mbar_wait(&ctl->r_full[kst], (e / NR) & 1, abort_flag) ||
+            !mbar_wait(&ctl->s1_empty[bsel], (n & 1) ^ 1, abort_flag))
+          return false;
         tc_fence_after();
-#pragma unroll
-        for (int t = 0; t < 2; ++t)
-          if (n_t[t] > 0) {
-            issue_s(t, 0);
-            mma_commit(&ctl->s_full[t]);
+        const uint32_t col = bsel ? C::kColO : C::kColS;
+        if (u < n_t[0]) issue_s(0, kst, col);
+        if (u < n_t[1]) issue_s(1, kst, col + 128);
+        mma_commit(&ctl->s1_full[bsel]);
+        mma_commit(&ctl->r_empty[kst]);
+        const uint32_t absent = (u < n_t[0] ? 0u : 4u) + (u < n_t[1] ? 0u : 4u);
+        if (absent != 0u) mbar_arrive_cnt(&ctl->s1_empty[bsel], absent);
+        return true;
+      };
+      if (warp == kWarpMma2) {
+        // odd tiles of the first chunk (ring entry = tile index there)
+        if (vote_pass) {
+          int n = 0;
+          for (int u = 1; ok && u < chunk_end(0); u += 2, ++n) ok = vote_tile(u, u, 1, n);
+        }
+        mma_commit(&ctl->mma_done2);
+        mbar_wait(&ctl->mma_done2, 0, nullptr);  // its MMAs are done before TMEM is freed
+      } else {
+      int rseq = 0;  // ring entries consumed
+      int s1cnt = 0;  // vote-pass uses of score buffer 0
+      int scnt[2] = {0, 0};
+      uint32_t o_acc[2] = {0u, 0u};
+      for (int c = 0; ok && c < nchunks; ++c) {
+        const int cb = chunk_begin(c), ce = chunk_end(c);
+        if (vote_pass) {
+          // ---- vote pass: every tile, both blocks, double-buffered scores.
+          // First chunk: even tiles here, odd ones in warp 9 (buffer 1 is
+          // O's columns, free until the first P.V); later chunks: every tile
+          // into buffer 0.
+          for (int u = cb; ok && u < ce; ++u) {
+            if (c == 0 && (u & 1)) continue;
+            ok = vote_tile(u, rseq + (u - cb), 0, s1cnt);
+            ++s1cnt;
           }
-        mma_commit(&ctl->k_empty[0]);
-      }
-      for (int i = 1; ok && i <= nmax; ++i) {
-        const int kst = i % NK, vst = (i - 1) % NV;
-        bool k_ready = false, v_ready = false, any_pv = false;
+          rseq += ce - cb;
+          if (!kPV || !ok) continue;
+          if (!mbar_wait(&ctl->votes_done[c & 1], (c >> 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+        }
+        // ---- compute pass: tiles kept by either block (ring entries K(u),
+        // V(u)), plus one trailing step for the last P.V MMAs.
+        bool prevk[2] = {false, false};
+        int prev_v = 0;  // ring entry of the previous tile's V
+        for (int u = next_kept(c, 2, cb);; u = next_kept(c, 2, u + 1)) {
+          const bool last = (u >= ce);
+          const int kst = rseq % NR, vst = prev_v % NR;
+          bool k_ready = false, v_ready = false, any_pv = false;
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (i - 1 < n_t[t]) {
-            // block t has read S_t(i-1) (and written P_t(i-1) if kept)
-            if (!mbar_wait(&ctl->p_full[t], (i - 1) & 1, abort_flag)) {
-              ok = false;
-              break;
-            }
-            if (kPV && *reinterpret_cast<volatile int*>(&ctl->dec[t])) {
+          for (int t = 0; t < 2; ++t) {
+            if (prevk[t]) {
+              // block t has written P_t for its previous kept tile
+              if (!mbar_wait(&ctl->p_full[t], (scnt[t] - 1) & 1, abort_flag)) {
+                ok = false;
+                break;
+              }
               if (!v_ready) {
-                if (!mbar_wait(&ctl->v_full[vst], ((i - 1) / NV) & 1, abort_flag)) {
+                if (!mbar_wait(&ctl->r_full[vst], (prev_v / NR) & 1, abort_flag)) {
                   ok = false;
                   break;
                 }
@@ -259,37 +383,32 @@ __global__ void __launch_bounds__(kThreads, 1)
               o_acc[t] = 1u;
               any_pv = true;
             }
-          }
-          if (i < n_t[t]) {
-            if (!k_ready) {
-              if (!mbar_wait(&ctl->k_full[kst], (i / NK) & 1, abort_flag)) {
-                ok = false;
-                break;
+            prevk[t] = !last && kept(c, t, u);
+            if (prevk[t]) {
+              if (!k_ready) {
+                if (!mbar_wait(&ctl->r_full[kst], (rseq / NR) & 1, abort_flag)) {
+                  ok = false;
+                  break;
+                }
+                k_ready = true;
               }
-              k_ready = true;
+              tc_fence_after();
+              issue_s(t, kst, C::kColS + 128 * t);
+              mma_commit(&ctl->s_full[t]);
+              ++scnt[t];
             }
-            tc_fence_after();
-            issue_s(t, kst);
-            mma_commit(&ctl->s_full[t]);
           }
+          if (!ok) break;
+          if (any_pv) mma_commit(&ctl->r_empty[vst]);  // V(prev) is free once its MMAs are done
+          if (last) break;
+          mma_commit(&ctl->r_empty[kst]);
+          prev_v = rseq + 1;
+          rseq += 2;
         }
-        if (!ok) break;
-        if (k_ready) mma_commit(&ctl->k_empty[kst]);
-        if (kPV) {
-          // V(i-1) is free once the MMAs reading it are done (or, if no block
-          // kept the tile, once its copy has landed).
-          if (any_pv) {
-            mma_commit(&ctl->v_empty[vst]);
-          } else {
-            if (!v_ready && !mbar_wait(&ctl->v_full[vst], ((i - 1) / NV) & 1, abort_flag)) {
-              ok = false;
-              break;
-            }
-            mbar_arrive(&ctl->v_empty[vst]);
-          }
-        }
+        if (use_masks) mbar_arrive(&ctl->mask_free[c & 1]);
       }
-      if (ok) mma_commit(&ctl->o_done);
+      if (kPV && ok) mma_commit(&ctl->o_done);
+      }
     }
     __syncwarp();
   }
@@ -299,19 +418,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     mma_commit(&ctl->mma_done);
     mbar_wait(&ctl->mma_done, 0, nullptr);
   }
-  if ((warp == kWarpK || warp == kWarpV) && lane == 0 && *abort_flag) {
+  if (warp == kWarpLoad && lane == 0 && *abort_flag) {
     // On an abort, let in-flight TMA writes land before shared memory is released.
-    // The newest load issued into stage s is the largest i < n with i % stages == s.
-    if (warp == kWarpK) {
-      if (nmax > 0) mbar_wait(&ctl->q_full, 0, nullptr);
-      for (int s = 0; s < NK; ++s)
-        if (n_k_issued > s)
-          mbar_wait(&ctl->k_full[s], ((s + ((n_k_issued - 1 - s) / NK) * NK) / NK) & 1, nullptr);
-    } else {
-      for (int s = 0; s < NV; ++s)
-        if (n_v_issued > s)
-          mbar_wait(&ctl->v_full[s], ((s + ((n_v_issued - 1 - s) / NV) * NV) / NV) & 1, nullptr);
-    }
+    // The newest entry issued into slot s is the largest e < n with e % NR == s.
+    if (nmax > 0) mbar_wait(&ctl->q_full, 0, nullptr);
+    for (int s = 0; s < NR; ++s)
+      if (n_issued > s)
+        mbar_wait(&ctl->r_full[s], ((s + ((n_issued - 1 - s) / NR) * NR) / NR) & 1, nullptr);
   }
   __syncwarp();
   tc_fence_before();
@@ -323,7 +436,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   } else {
     // ---------------------------------------------------------- softmax (block t)
-    setmaxnreg_inc<kRegsSoftmax>();
+    constexpr uint32_t kRegsUp = kRegsSoftmax<MODE>;
+    setmaxnreg_inc<kRegsUp>();
     const int t = warp >> 2;
     const int tid_t = tid & 127;
     const int row = tid_t;
@@ -344,108 +458,167 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_true = -INFINITY, m_used = -INFINITY, l = 0.f;
     uint32_t skipped = 0;
     bool ok = true;
+    int n1[2] = {0, 0}, n2 = 0;
     // Warp-uniform waits: tcgen05.ld/st are warp-collective, so a failed wait
     // ends the loop for the whole warp; the other warps then time out too.
     auto wwait = [&](uint64_t* bar, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
     };
-
-    // Vote path: the block's four warps meet at named barrier 2 + t once per
-    // tile (bar.red), and no thread may skip it -- a failed wait is carried
-    // to the barrier and the warps leave the loop together.  The dense path
-    // has no barrier inside the loop and leaves on its own.
-    const bool team = kVote || p.margin != nullptr;
-    const uint32_t bar_id = 2 + t;
-    for (int i = 0; i < n_mine; ++i) {
-      const bool got = wwait(&ctl->s_full[t], i & 1);
-      if (!got && !team) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
+    // Masked scores of tile i in registers (one TMEM round trip) and the row
+    // maximum (four independent partial maxima).
+    auto load_scores = [&](uint32_t col, int i, uint32_t (&sr)[128], bool want_max) -> float {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32p(col + 32 * c, sr + 32 * c);
+      tmem_wait_ld();
       const long k0 = static_cast<long>(i) * kTile;
       const bool full = (k0 + kTile - 1 <= lim);
       // last visible column of this tile for this row (-1: none), 32-bit
       const int vis = static_cast<int>(max(-1L, min(static_cast<long>(kTile - 1), lim - k0)));
-
-      // All 128 scores of the row in registers (one TMEM round trip); masked
-      // keys become -inf; four independent partial maxima.
-      uint32_t sr[128];
-      if (got) {
+      if (!full) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32p(colS + 32 * c, sr + 32 * c);
-        tmem_wait_ld();
-      } else {
-#pragma unroll
-        for (int e = 0; e < 128; ++e) sr[e] = __float_as_uint(-INFINITY);
+        for (int e = 0; e < 128; ++e)
+          if (e > vis) sr[e] = __float_as_uint(-INFINITY);
       }
+      if (!want_max) return 0.f;
       float mx[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) mx[e] = -INFINITY;
-      if (full) {
 #pragma unroll
-        for (int e = 0; e < 128; ++e) mx[e & 3] = fmaxf(mx[e & 3], __uint_as_float(sr[e]));
-      } else {
-#pragma unroll
-        for (int e = 0; e < 128; ++e) {
-          if (e > vis) sr[e] = __float_as_uint(-INFINITY);
-          mx[e & 3] = fmaxf(mx[e & 3], __uint_as_float(sr[e]));
-        }
-      }
-      const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      for (int e = 0; e < 128; ++e) mx[e & 3] = fmaxf(mx[e & 3], __uint_as_float(sr[e]));
+      return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+    };
+    const uint32_t bar_id = 2 + t;
 
-      // Skip vote: every row of the block must pass exp(scale*(tmax - m)) < lambda.
-      // (The dense path runs the same reduction only to report margins.)
-      bool skip = false;
-      if (team) {
-        float c_r = -INFINITY;  // a row with no visible key does not veto
-        if (tmax != -INFINITY) c_r = (m_true == -INFINITY) ? INFINITY : tmax - m_true;
-        const bool all_pass = named_bar_and(bar_id, 128, got && c_r < p.thr_raw);
-        if (!all_pass && named_bar_or(bar_id, 128, !got)) {
+    for (int c = 0; c < nchunks; ++c) {
+      const int cb = chunk_begin(c);
+      const int ce = min(chunk_end(c), n_mine);
+      if (vote_pass) {
+        // ---------------------------------------------- vote pass (chunk c)
+        bool mf_ok = true;
+        if (use_masks && tid_t == 0) {
+          // the chunk parity's masks are free once chunk c-2's readers are done
+          if (c >= 2) mf_ok = mbar_wait(&ctl->mask_free[c & 1], ((c >> 1) - 1) & 1, abort_flag);
+          for (int w = 0; w < kMaskWords; ++w) ctl->kmask[c & 1][t][w] = 0u;
+        }
+        // The block's four warps meet at named barrier 2 + t once per tile
+        // (bar.red), and no thread may skip it: a failed wait is carried to
+        // the barrier and the warps leave the loop together.
+        for (int i = cb; i < ce; ++i) {
+          const int bsel = (c == 0) ? (i & 1) : 0;
+          const bool got = wwait(&ctl->s1_full[bsel], (bsel ? n1[1] : n1[0]) & 1);
+          if (bsel) ++n1[1]; else ++n1[0];
+          tc_fence_after();
+          uint32_t sr[128];
+          float tmax = -INFINITY;
+          if (got) tmax = load_scores(lane_base + (bsel ? C::kColO : C::kColS) + 128 * t, i, sr, true);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ctl->s1_empty[bsel]);
+
+          // Skip vote: every row of the block must pass exp(scale*(tmax - m)) < lambda.
+          // (The dense path runs the same reduction only to report margins.)
+          float c_r = -INFINITY;  // a row with no visible key does not veto
+          if (tmax != -INFINITY) c_r = (m_true == -INFINITY) ? INFINITY : tmax - m_true;
+          const bool all_pass = named_bar_and(bar_id, 128, got && c_r < p.thr_raw);
+          if (!all_pass && named_bar_or(bar_id, 128, !got)) {
+            ok = false;
+            break;
+          }
+          const bool skip = kVote && all_pass;
+          if (p.margin != nullptr) {
+            float cm = c_r;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
+            if (lane == 0) *reinterpret_cast<volatile float*>(&ctl->red[t][i & 1][warp & 3]) = cm;
+            named_bar_sync(bar_id, 128);
+            if (tid_t == 0) {
+              const volatile float* rr = ctl->red[t][i & 1];
+              const float cmax = fmaxf(fmaxf(rr[0], rr[1]), fmaxf(rr[2], rr[3]));
+              p.margin[unit * p.nT + i] = (cmax == INFINITY) ? INFINITY : cmax * p.scale;
+            }
+          }
+          m_true = fmaxf(m_true, tmax);
+          if (tid_t == 0) {
+            skipped += skip ? 1u : 0u;
+            if (p.mask != nullptr) p.mask[unit * p.nT + i] = skip ? 1 : 0;
+            if (use_masks && !skip) {
+              const int r = i - cb;
+              ctl->kmask[c & 1][t][r >> 5] |= 1u << (r & 31);
+            }
+          }
+        }
+        // Masks of this chunk are complete: the producers and the MMA issuer
+        // may walk them; the block's own threads read them after the barrier.
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ctl->votes_done[c & 1]);
+        if (!kPV) {
+          if (!ok) break;  // block-uniform: vote-pass failures leave through bar.red.or
+          continue;
+        }
+        // Block-uniform exit on any failure so far; also publishes the masks.
+        if (named_bar_or(bar_id, 128, !(ok && mf_ok))) {
           ok = false;
           break;
         }
-        skip = kVote && all_pass;
-        if (p.margin != nullptr) {
-          float cm = c_r;
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
-          if (lane == 0) *reinterpret_cast<volatile float*>(&ctl->red[t][i & 1][warp & 3]) = cm;
-          named_bar_sync(bar_id, 128);
-          if (tid_t == 0) {
-            const volatile float* rr = ctl->red[t][i & 1];
-            const float cmax = fmaxf(fmaxf(rr[0], rr[1]), fmaxf(rr[2], rr[3]));
-            p.margin[unit * p.nT + i] = (cmax == INFINITY) ? INFINITY : cmax * p.scale;
-          }
-        }
-      }
-      m_true = fmaxf(m_true, tmax);
-      if (tid_t == 0) {
-        skipped += skip ? 1u : 0u;
-        if (p.mask != nullptr) p.mask[unit * p.nT + i] = skip ? 1 : 0;
-      }
-
-      if (kPV && !skip) {
-        // O_t may be touched: the commit behind s_full covers P.V of tile i-1.
+        // Known maxima: the compute pass uses the exact row maximum so far.
+        // A later chunk that raised it rescales O and l once (every earlier
+        // P.V is complete: the vote-pass scores waited on came after them).
         float alpha = 1.f;
         bool need_rescale = false;
-        if (m_used == -INFINITY) {
-          m_used = m_true;  // first visible key of this row: its O row is still zero
-        } else if ((m_true - m_used) * sl2 > kRescaleLog2) {
+        if (m_used != -INFINITY && m_true > m_used) {
           alpha = ex2_approx((m_used - m_true) * sl2);
           need_rescale = true;
-          m_used = m_true;
           l *= alpha;
         }
         if (__any_sync(0xffffffffu, need_rescale)) {
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
+#pragma unroll 1
+          for (int cc = 0; cc < D / 32; ++cc) {
             uint32_t orr[32];
-            tmem_ld32p(colO + c * 32, orr);
+            tmem_ld32p(colO + cc * 32, orr);
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
-            tmem_st32p(colO + c * 32, orr);
+            tmem_st32p(colO + cc * 32, orr);
+          }
+          tmem_wait_st();
+        }
+        m_used = m_true;
+      }
+
+      // ---------------------------------------------- compute pass (chunk c)
+      for (int i = next_kept(c, t, cb); i < ce; i = next_kept(c, t, i + 1)) {
+        if (!wwait(&ctl->s_full[t], n2 & 1)) {
+          ok = false;
+          break;
+        }
+        ++n2;
+        tc_fence_after();
+        uint32_t sr[128];
+        const float tmax = load_scores(colS, i, sr, !vote_pass);
+        if (!vote_pass) {
+          // Dense path: online maximum with a lazy O rescale.
+          m_true = fmaxf(m_true, tmax);
+          float alpha = 1.f;
+          bool need_rescale = false;
+          if (m_used == -INFINITY) {
+            m_used = m_true;  // first visible key of this row: its O row is still zero
+          } else if ((m_true - m_used) * sl2 > kRescaleLog2) {
+            alpha = ex2_approx((m_used - m_true) * sl2);
+            need_rescale = true;
+            m_used = m_true;
+            l *= alpha;
+          }
+          if (__any_sync(0xffffffffu, need_rescale)) {
+            // O_t may be touched: the commit behind s_full covers P.V of the previous tile.
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+              uint32_t orr[32];
+              tmem_ld32p(colO + cc * 32, orr);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+              tmem_st32p(colO + cc * 32, orr);
+            }
           }
         }
         // P = exp2(s*scale*log2e - m) packed in place as bf16 pairs, then
@@ -455,20 +628,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 4; ++e) ls[e] = 0.f;
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * c]), sl2, -mb));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * c + 1]), sl2, -mb));
-          ls[c & 3] += p0 + p1;
-          sr[c] = pack_bf16x2(p0, p1);
+        for (int cc = 0; cc < 64; ++cc) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * cc]), sl2, -mb));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * cc + 1]), sl2, -mb));
+          ls[cc & 3] += p0 + p1;
+          sr[cc] = pack_bf16x2(p0, p1);
         }
         tmem_st32p(colS, sr);
         tmem_st32p(colS + 32, sr + 32);
         tmem_wait_st();
         l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        tc_fence_before();
+        mbar_arrive(&ctl->p_full[t]);
       }
-      tc_fence_before();
-      if (tid_t == 0) *reinterpret_cast<volatile int*>(&ctl->dec[t]) = skip ? 0 : 1;
-      mbar_arrive(&ctl->p_full[t]);
+      // Another chunk's vote pass meets at the named barrier again: leave
+      // together if any warp of the block failed.
+      if (vote_pass && c + 1 < nchunks && named_bar_or(bar_id, 128, !ok)) {
+        ok = false;
+        break;
+      }
+      if (!ok) break;
     }
 
     if (kPV && ok && n_mine > 0) {

@@ -123,6 +123,11 @@ ss_status prefill_impl(const void* q, const void* k, const void* v, void* o, int
   p.nQB = static_cast<int>(nQB);
   p.nT = static_cast<int>(nT);
   p.causal = causal ? 1 : 0;
+  p.chunk_tiles = kVoteChunkTiles;
+  if (dbg != nullptr && dbg->vote_chunk_tiles != 0) {
+    if (dbg->vote_chunk_tiles < 1 || dbg->vote_chunk_tiles > kVoteChunkTiles) return SS_ERR_INVALID_ARG;
+    p.chunk_tiles = dbg->vote_chunk_tiles;
+  }
   p.scale = scale;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   p.thr_raw = thr_raw;
@@ -131,7 +136,11 @@ ss_status prefill_impl(const void* q, const void* k, const void* v, void* o, int
   p.mask = dbg ? dbg->skip_mask : nullptr;
   p.margin = dbg ? dbg->vote_margin : nullptr;
   p.status = status_ptr();
-  const Mode mode = count_only ? Mode::kCount : (dense ? Mode::kDense : Mode::kSparse);
+  // lambda = 0 with skip masks or margins requested runs the voting kernel
+  // with a threshold no tile passes (every tile kept, margins reported).
+  const bool debug_out = p.mask != nullptr || p.margin != nullptr;
+  const Mode mode =
+      count_only ? Mode::kCount : ((dense && !debug_out) ? Mode::kDense : Mode::kSparse);
   cudaError_t e = launch_prefill(d, mode, tq, tk, tv, p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }

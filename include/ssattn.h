@@ -89,6 +89,12 @@ typedef struct {
      land, returns, and ss_stream_status() reports SS_ERR_TIMEOUT.  The
      output is unspecified; the context stays usable. */
   int fault_inject;
+  /* Test only, prefill only (0 otherwise).  The prefill kernel decides a
+     run of key tiles (by default 2048) before it computes the run's kept
+     tiles, and carries the softmax state from run to run; a value in
+     [1, 2048] shortens the run so that short inputs take the multi-run
+     path.  Results do not depend on it (up to rounding). */
+  int vote_chunk_tiles;
 } ss_debug_opts;
 
 /*

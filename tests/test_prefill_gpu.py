@@ -51,6 +51,27 @@ def test_ragged_shapes(shape, lam_kind):
     check_prefill(inp.q, inp.k, inp.v, scale=1.0 / math.sqrt(d), causal=causal, lam=lam)
 
 
+CHUNKED = [
+    # B, Hq, Hkv, Lq, Lk, d, causal, vote-run length in tiles
+    (1, 2, 1, 700, 1500, 128, False, 3),   # 12 tiles in runs of 3
+    (1, 2, 2, 1500, 1500, 64, True, 1),    # one tile per run: every raised max rescales O
+    (2, 4, 2, 300, 2100, 128, True, 5),    # Lq < Lk causal, ragged last run
+]
+
+
+@pytest.mark.parametrize("shape", CHUNKED)
+@pytest.mark.parametrize("a", [1.0, 16.0])
+def test_multi_run_votes(shape, a):
+    """Inputs longer than one vote run (2048 tiles) decide and compute run by
+    run; a short run length (test-only option) takes that path at small sizes."""
+    from _parity import check_prefill, hot_prefill
+
+    B, Hq, Hkv, Lq, Lk, d, causal, chunk = shape
+    inp = hot_prefill(B, Hq, Hkv, Lq, Lk, d, frac=0.25, seed=7)
+    check_prefill(inp.q, inp.k, inp.v, scale=1.0 / math.sqrt(d), causal=causal,
+                  lam=min(1.0, a / Lk), chunk=chunk)
+
+
 def test_random_scores_many_decisions():
     """Plain N(0,1) inputs (no planted structure): margins spread out, so many
     tiles sit near the threshold -- exercises the near-margin accounting."""
