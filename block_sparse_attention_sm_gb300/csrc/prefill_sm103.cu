@@ -34,12 +34,13 @@
 //   warp 8           TMA producer: both Q blocks, then one FIFO ring of
 //                    tiles: K of every tile (vote pass), then K and V of the
 //                    kept tiles (compute pass).
-//   warp 10          TMEM allocator + single-thread tcgen05 MMA issuer.  Vote
-//                    pass: S_0(i), S_1(i) into score buffer i % 2, one
-//                    commit for both.
-//                    Compute pass, over the tiles kept by either block:
-//                    ... PV_0(prev), S_0(u), PV_1(prev), S_1(u) ... so one
-//                    block's softmax overlaps the other block's MMAs.
+//   warps 9, 10      tcgen05 MMA issuers (one thread each; warp 10 also
+//                    allocates TMEM).  Vote pass: S_0(i), S_1(i) into score
+//                    buffer i % 2, one commit for both; the first chunk's
+//                    even / odd tiles come from warp 10 / 9.  Compute pass:
+//                    warp 10 issues block 0's PV_0(prev), S_0(u) ..., warp 9
+//                    block 1's, each as its softmax frees S, so one block's
+//                    softmax overlaps the other block's MMAs.
 //                    S_t = Q_t K^T: SS form, both operands K-major, 128-byte
 //                    swizzle.  O_t += P_t V: TS form, P_t from TMEM, V MN-major.
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256, 256+d),
@@ -59,7 +60,7 @@ namespace {
 constexpr float kRescaleLog2 = 8.0f;  // lazy-rescale slack of the dense path, exp2 domain
 constexpr int kThreads = 384;         // three warpgroups
 constexpr int kWarpLoad = 8, kWarpMma = 10;  // warp 11 idles
-constexpr int kWarpMma2 = 9;  // second score issuer of the vote pass
+constexpr int kWarpMma2 = 9;  // MMA issuer of query block 1
 // Register split: launched at 168 per thread (384 x 168 = 64512); the
 // producer/MMA warpgroup drops to kRegsIssue and the two softmax warpgroups
 // rise to kRegsSoftmax, with 128 x issue + 256 x softmax = 64512, i.e.
@@ -113,11 +114,13 @@ struct PrefillCtl {
   // that a reader one chunk behind (the V producer, when a chunk keeps no
   // tile) never sees a phase two chunks ahead.
   uint64_t votes_done[2];
-  uint64_t mask_free[2];                   // per chunk parity: its 2 readers are done
-  uint64_t o_done;
-  uint64_t mma_done, mma_done2;
+  uint64_t mask_free[2];                   // per chunk parity: its 3 readers are done
+  uint64_t o_done[2];                      // per block: its last P.V is done
+  uint64_t c1_done;                        // per chunk: block 1's compute MMAs are done
+  uint64_t mma_done[2];                    // per issuing thread, for teardown
   uint32_t tmem_base;
   int abort_flag;
+  int n_loaded;  // ring entries whose copy has been issued (monotone)
   float red[2][2][4];
   uint32_t kmask[2][2][kMaskWords];  // kept tiles: [chunk parity][block][bit]
 };
@@ -203,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&ctl->q_full, 1);
     for (int s = 0; s < NR; ++s) {
       mbar_init(&ctl->r_full[s], 1);
-      mbar_init(&ctl->r_empty[s], 1);
+      mbar_init(&ctl->r_empty[s], MODE == Mode::kDense ? 1 : 2);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&ctl->s1_full[t], 1);
@@ -213,12 +216,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&ctl->votes_done[0], 8);
     mbar_init(&ctl->votes_done[1], 8);
-    mbar_init(&ctl->mask_free[0], 2);
-    mbar_init(&ctl->mask_free[1], 2);
-    mbar_init(&ctl->o_done, 1);
-    mbar_init(&ctl->mma_done, 1);
-    mbar_init(&ctl->mma_done2, 1);
+    mbar_init(&ctl->mask_free[0], 3);
+    mbar_init(&ctl->mask_free[1], 3);
+    mbar_init(&ctl->o_done[0], 1);
+    mbar_init(&ctl->o_done[1], 1);
+    mbar_init(&ctl->c1_done, 1);
+    mbar_init(&ctl->mma_done[0], 1);
+    mbar_init(&ctl->mma_done[1], 1);
     ctl->abort_flag = 0;
+    ctl->n_loaded = 0;
     fence_mbar_init();
   }
   if (warp == kWarpMma) {
@@ -261,6 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(sR + st * C::kTileBytes + c * 16384, map, &ctl->r_full[st], c * 64,
                       u * kTile, zk);
         ++n_issued;
+        *reinterpret_cast<volatile int*>(&ctl->n_loaded) = n_issued;
         return true;
       };
       bool ok = true;
@@ -278,11 +285,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kWarpMma || warp == kWarpMma2) {
     // ---------------------------------------------------------- MMA issuers
     // Issuing blocks until the tensor pipe takes each MMA, so the pipe idles
-    // while its issuer waits or commits.  In the first chunk's vote pass two
-    // threads issue the score MMAs -- even tiles into score buffer 0 (warp
-    // 10), odd tiles into buffer 1 (warp 9) -- so one keeps the pipe fed
-    // while the other synchronises.  Warp 10 issues everything else.
+    // while its issuer waits or commits.  Two threads issue: warp 10 the
+    // MMAs of query block 0, warp 9 those of block 1 (compute pass), and in
+    // the first chunk's vote pass the even / odd tiles into score buffer
+    // 0 / 1; one keeps the pipe fed while the other synchronises.  Later
+    // chunks' vote passes (score buffer 0 only) are issued by warp 10.
     if (lane == 0 && nmax > 0) {
+      const int tb = (warp == kWarpMma) ? 0 : 1;
       constexpr uint32_t idS = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t idO = idesc_bf16_f32(128, D, false, true);
       const uint32_t sQa = smem_u32(sQ), sRa = smem_u32(sR);
@@ -306,46 +315,66 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_bf16_ts(tmem + C::kColO + 128 * t, tmem + C::kColS + 128 * t + kk * 8,
                       dv + ((kk * 2048) >> 4), idO, (acc | kk) ? 1u : 0u);
       };
+      // Voting kernels: a ring slot is free after two arrivals, one commit
+      // per block whose MMAs read it; a block that reads it alone adds the
+      // second arrival itself (after its wait for the slot's data, so in the
+      // right phase).  Dense kernel: one thread issues every read, one commit.
+      auto release = [&](int st, bool alone) {
+        mma_commit(&ctl->r_empty[st]);
+        if (MODE != Mode::kDense && alone) mbar_arrive(&ctl->r_empty[st]);
+      };
       bool ok = mbar_wait(&ctl->q_full, 0, abort_flag);
+      // Wait for ring entry e's data.  The two issuers consume different
+      // subsets of the ring, so one may ask for an entry the producer has not
+      // reached; a parity wait alone could then see the slot's previous
+      // phase.  Waiting first until the copy of e has been issued pins the
+      // slot's barrier to e's phase (e's slot cannot be reused before this
+      // thread releases e).
+      auto ring_wait = [&](int e) -> bool {
+        if (*reinterpret_cast<volatile int*>(&ctl->n_loaded) <= e) {
+          const uint64_t t0 = globaltimer_ns();
+          while (*reinterpret_cast<volatile int*>(&ctl->n_loaded) <= e) {
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+              *abort_flag = 1;
+              return false;
+            }
+          }
+        }
+        return mbar_wait(&ctl->r_full[e % NR], (e / NR) & 1, abort_flag);
+      };
       // One vote-pass tile: ring entry `e`, score buffer `bsel`, `n` earlier uses of it.
       auto vote_tile = [&](int u, int e, int bsel, int n) -> bool {
         const int kst = e % NR;
-        if (!mbar_wait(&ctl->r_full[kst], (e / NR) & 1, abort_flag) ||
-            !mbar_wait(&ctl->s1_empty[bsel], (n & 1) ^ 1, abort_flag))
+        if (!ring_wait(e) || !mbar_wait(&ctl->s1_empty[bsel], (n & 1) ^ 1, abort_flag))
           return false;
         tc_fence_after();
         const uint32_t col = bsel ? C::kColO : C::kColS;
         if (u < n_t[0]) issue_s(0, kst, col);
         if (u < n_t[1]) issue_s(1, kst, col + 128);
         mma_commit(&ctl->s1_full[bsel]);
-        mma_commit(&ctl->r_empty[kst]);
+        release(kst, true);
         const uint32_t absent = (u < n_t[0] ? 0u : 4u) + (u < n_t[1] ? 0u : 4u);
         if (absent != 0u) mbar_arrive_cnt(&ctl->s1_empty[bsel], absent);
         return true;
       };
-      if (warp == kWarpMma2) {
-        // odd tiles of the first chunk (ring entry = tile index there)
-        if (vote_pass) {
-          int n = 0;
-          for (int u = 1; ok && u < chunk_end(0); u += 2, ++n) ok = vote_tile(u, u, 1, n);
-        }
-        mma_commit(&ctl->mma_done2);
-        mbar_wait(&ctl->mma_done2, 0, nullptr);  // its MMAs are done before TMEM is freed
-      } else {
-      int rseq = 0;  // ring entries consumed
-      int s1cnt = 0;  // vote-pass uses of score buffer 0
-      int scnt[2] = {0, 0};
-      uint32_t o_acc[2] = {0u, 0u};
+      int rseq = 0;    // ring entries of the chunks before (both threads track it)
+      int s1cnt = 0;   // vote-pass uses of this thread's score buffer
+      int scnt = 0;    // compute-pass S MMAs of block tb
+      uint32_t o_acc = 0u;
       for (int c = 0; ok && c < nchunks; ++c) {
         const int cb = chunk_begin(c), ce = chunk_end(c);
         if (vote_pass) {
-          // ---- vote pass: every tile, both blocks, double-buffered scores.
-          // First chunk: even tiles here, odd ones in warp 9 (buffer 1 is
-          // O's columns, free until the first P.V); later chunks: every tile
-          // into buffer 0.
+          // ---- vote pass: every tile, both blocks, double-buffered scores
+          // Block 1's last compute MMAs of the previous chunk read its S
+          // columns, which this chunk's scores overwrite.
+          if (tb == 0 && kPV && c > 0 && !mbar_wait(&ctl->c1_done, (c - 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
           for (int u = cb; ok && u < ce; ++u) {
-            if (c == 0 && (u & 1)) continue;
-            ok = vote_tile(u, rseq + (u - cb), 0, s1cnt);
+            if (c == 0 ? ((u & 1) != tb) : (tb != 0)) continue;
+            ok = vote_tile(u, rseq + (u - cb), c == 0 ? tb : 0, s1cnt);
             ++s1cnt;
           }
           rseq += ce - cb;
@@ -355,69 +384,109 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
         }
-        // ---- compute pass: tiles kept by either block (ring entries K(u),
-        // V(u)), plus one trailing step for the last P.V MMAs.
-        bool prevk[2] = {false, false};
-        int prev_v = 0;  // ring entry of the previous tile's V
-        for (int u = next_kept(c, 2, cb);; u = next_kept(c, 2, u + 1)) {
-          const bool last = (u >= ce);
-          const int kst = rseq % NR, vst = prev_v % NR;
-          bool k_ready = false, v_ready = false, any_pv = false;
+        if constexpr (MODE == Mode::kDense) {
+          // ---- dense: one thread issues both blocks' MMAs in the order
+          // PV_0(i-1), S_0(i), PV_1(i-1), S_1(i), which keeps the two blocks'
+          // softmaxes alternating (ring entries K(i), V(i); one trailing step).
+          // A single consumer takes the ring in order: plain parity waits.
+          if (tb == 0) {
+            bool prevk[2] = {false, false};
+            int prev_ve = 0;
+            uint32_t oacc[2] = {0u, 0u};
+            int sc[2] = {0, 0};
+            for (int u = cb;; ++u) {
+              const bool last = (u >= ce);
+              const int ke = rseq + 2 * (u - cb), kst = ke % NR, vst = prev_ve % NR;
+              bool k_ready = false, v_ready = false, any_pv = false;
 #pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            if (prevk[t]) {
-              // block t has written P_t for its previous kept tile
-              if (!mbar_wait(&ctl->p_full[t], (scnt[t] - 1) & 1, abort_flag)) {
-                ok = false;
-                break;
-              }
-              if (!v_ready) {
-                if (!mbar_wait(&ctl->r_full[vst], (prev_v / NR) & 1, abort_flag)) {
-                  ok = false;
-                  break;
+              for (int t = 0; t < 2; ++t) {
+                if (prevk[t]) {
+                  if (!mbar_wait(&ctl->p_full[t], (sc[t] - 1) & 1, abort_flag) ||
+                      (!v_ready && !mbar_wait(&ctl->r_full[vst], (prev_ve / NR) & 1, abort_flag))) {
+                    ok = false;
+                    break;
+                  }
+                  v_ready = true;
+                  tc_fence_after();
+                  issue_pv(t, vst, oacc[t]);
+                  oacc[t] = 1u;
+                  any_pv = true;
                 }
-                v_ready = true;
-              }
-              tc_fence_after();
-              issue_pv(t, vst, o_acc[t]);
-              o_acc[t] = 1u;
-              any_pv = true;
-            }
-            prevk[t] = !last && kept(c, t, u);
-            if (prevk[t]) {
-              if (!k_ready) {
-                if (!mbar_wait(&ctl->r_full[kst], (rseq / NR) & 1, abort_flag)) {
-                  ok = false;
-                  break;
+                prevk[t] = !last && u < n_t[t];
+                if (prevk[t]) {
+                  if (!k_ready && !mbar_wait(&ctl->r_full[kst], (ke / NR) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                  }
+                  k_ready = true;
+                  tc_fence_after();
+                  issue_s(t, kst, C::kColS + 128 * t);
+                  mma_commit(&ctl->s_full[t]);
+                  ++sc[t];
                 }
-                k_ready = true;
               }
-              tc_fence_after();
-              issue_s(t, kst, C::kColS + 128 * t);
-              mma_commit(&ctl->s_full[t]);
-              ++scnt[t];
+              if (!ok) break;
+              if (any_pv) release(vst, true);  // one thread covers both blocks' reads
+              if (last) break;
+              release(kst, true);
+              prev_ve = ke + 1;
             }
+            if (ok) mma_commit(&ctl->o_done[1]);
           }
-          if (!ok) break;
-          if (any_pv) mma_commit(&ctl->r_empty[vst]);  // V(prev) is free once its MMAs are done
-          if (last) break;
-          mma_commit(&ctl->r_empty[kst]);
-          prev_v = rseq + 1;
-          rseq += 2;
+        } else {
+          // ---- compute pass of block tb over the tiles kept by either block
+          // (ring entries K(u), V(u) in that order).
+          bool have_prev = false, prev_alone = false;
+          int prev_ve = 0;  // ring entry of the previous kept tile's V
+          auto pv_prev = [&]() -> bool {
+            const int vst = prev_ve % NR;
+            if (!mbar_wait(&ctl->p_full[tb], (scnt - 1) & 1, abort_flag) || !ring_wait(prev_ve))
+              return false;
+            tc_fence_after();
+            issue_pv(tb, vst, o_acc);
+            o_acc = 1u;
+            release(vst, prev_alone);
+            return true;
+          };
+          int k = 0;
+          for (int u = next_kept(c, 2, cb); ok && u < ce; u = next_kept(c, 2, u + 1), ++k) {
+            if (!kept(c, tb, u)) continue;
+            const int ke = rseq + 2 * k, kst = ke % NR;
+            const bool alone = !kept(c, 1 - tb, u);
+            if (have_prev && !pv_prev()) {
+              ok = false;
+              break;
+            }
+            if (!ring_wait(ke)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(tb, kst, C::kColS + 128 * tb);
+            mma_commit(&ctl->s_full[tb]);
+            release(kst, alone);
+            ++scnt;
+            have_prev = true;
+            prev_ve = ke + 1;
+            prev_alone = alone;
+          }
+          if (ok && have_prev && !pv_prev()) ok = false;
         }
+        if (!ok) break;
+        // the ring entries of this chunk's compute pass (count the whole list)
+        for (int u = next_kept(c, 2, cb); u < ce; u = next_kept(c, 2, u + 1)) rseq += 2;
+        if (tb == 1 && kPV && vote_pass && c + 1 < nchunks) mma_commit(&ctl->c1_done);
         if (use_masks) mbar_arrive(&ctl->mask_free[c & 1]);
       }
-      if (kPV && ok) mma_commit(&ctl->o_done);
-      }
+      // (Dense: warp 10 issued block 1's MMAs too and has committed its o_done.)
+      if (kPV && ok && !(MODE == Mode::kDense && tb == 1)) mma_commit(&ctl->o_done[tb]);
+      // Every MMA this thread issued must have finished before TMEM is freed.
+      mma_commit(&ctl->mma_done[tb]);
+      mbar_wait(&ctl->mma_done[tb], 0, nullptr);
     }
     __syncwarp();
   }
   // ------------------------------------------------------------ teardown (warps 8-11)
-  if (warp == kWarpMma && lane == 0 && nmax > 0) {
-    // Every MMA this thread issued must have finished before TMEM is freed.
-    mma_commit(&ctl->mma_done);
-    mbar_wait(&ctl->mma_done, 0, nullptr);
-  }
   if (warp == kWarpLoad && lane == 0 && *abort_flag) {
     // On an abort, let in-flight TMA writes land before shared memory is released.
     // The newest entry issued into slot s is the largest e < n with e % NR == s.
@@ -651,7 +720,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     if (kPV && ok && n_mine > 0) {
-      ok = wwait(&ctl->o_done, 0);
+      ok = wwait(&ctl->o_done[t], 0);
       tc_fence_after();
     }
     if (kPV && ok && rows_t > 0) {
