@@ -553,7 +553,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int e = 0; e < 4; ++e) mx[e] = -INFINITY;
 #pragma unroll
-      for (int e = 0; e < 128; ++e) mx[e & 3] = fmaxf(mx[e & 3], __uint_as_float(sr[e]));
+      for (int e = 0; e < 64; ++e)
+        mx[e & 3] = fmax3(mx[e & 3], __uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1]));
       return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
     };
     const uint32_t bar_id = 2 + t;
@@ -693,20 +694,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P = exp2(s*scale*log2e - m) packed in place as bf16 pairs, then
         // written over the first 64 columns of S (already read).
         const float mb = (m_used == -INFINITY) ? 0.f : m_used * sl2;
-        float ls[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) ls[e] = 0.f;
+        const uint64_t sl2x2 = f32x2(sl2, sl2), nmb = f32x2(-mb, -mb);
+        uint64_t ls[2] = {0ull, 0ull};  // +0.0 pairs
 #pragma unroll
         for (int cc = 0; cc < 64; ++cc) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * cc]), sl2, -mb));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * cc + 1]), sl2, -mb));
-          ls[cc & 3] += p0 + p1;
+          const uint64_t xp = fma_f32x2(f32x2(__uint_as_float(sr[2 * cc]), __uint_as_float(sr[2 * cc + 1])),
+                                        sl2x2, nmb);
+          const float p0 = ex2_approx(f32x2_lo(xp));
+          const float p1 = ex2_approx(f32x2_hi(xp));
+          ls[cc & 1] = add_f32x2(ls[cc & 1], f32x2(p0, p1));
           sr[cc] = pack_bf16x2(p0, p1);
         }
         tmem_st32p(colS, sr);
         tmem_st32p(colS + 32, sr + 32);
         tmem_wait_st();
-        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        const uint64_t lsum = add_f32x2(ls[0], ls[1]);
+        l += f32x2_lo(lsum) + f32x2_hi(lsum);
         tc_fence_before();
         mbar_arrive(&ctl->p_full[t]);
       }
