@@ -330,14 +330,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       // phase.  Waiting first until the copy of e has been issued pins the
       // slot's barrier to e's phase (e's slot cannot be reused before this
       // thread releases e).
+      int seen_loaded = 0;  // last value of n_loaded this thread read
       auto ring_wait = [&](int e) -> bool {
-        if (*reinterpret_cast<volatile int*>(&ctl->n_loaded) <= e) {
-          const uint64_t t0 = globaltimer_ns();
-          while (*reinterpret_cast<volatile int*>(&ctl->n_loaded) <= e) {
-            if (*abort_flag) return false;
-            if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
-              *abort_flag = 1;
-              return false;
+        if (seen_loaded <= e) {
+          seen_loaded = *reinterpret_cast<volatile int*>(&ctl->n_loaded);
+          if (seen_loaded <= e) {
+            const uint64_t t0 = globaltimer_ns();
+            while ((seen_loaded = *reinterpret_cast<volatile int*>(&ctl->n_loaded)) <= e) {
+              if (*abort_flag) return false;
+              if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+                *abort_flag = 1;
+                return false;
+              }
             }
           }
         }
@@ -625,6 +629,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;  // block-uniform: vote-pass failures leave through bar.red.or
           continue;
         }
+        // Wait until both blocks have voted: a block with fewer (or no) tiles
+        // would otherwise run ahead and arrive for chunk c + 2 while chunk c's
+        // phase of the same barrier is still open, completing it early.
+        if (!wwait(&ctl->votes_done[c & 1], (c >> 1) & 1)) ok = false;
         // Block-uniform exit on any failure so far; also publishes the masks.
         if (named_bar_or(bar_id, 128, !(ok && mf_ok))) {
           ok = false;

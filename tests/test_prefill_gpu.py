@@ -56,6 +56,9 @@ CHUNKED = [
     (1, 2, 1, 700, 1500, 128, False, 3),   # 12 tiles in runs of 3
     (1, 2, 2, 1500, 1500, 64, True, 1),    # one tile per run: every raised max rescales O
     (2, 4, 2, 300, 2100, 128, True, 5),    # Lq < Lk causal, ragged last run
+    # 3 query blocks: one CTA's second block is empty and races through the
+    # runs; the other block's votes must still gate every run (regression case)
+    (2, 4, 2, 384, 2100, 128, False, 5),
 ]
 
 
