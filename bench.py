@@ -501,13 +501,78 @@ def run_suite(args):
         del res
         torch.cuda.empty_cache()
 
-    prefill_points("tiny_prefill", [0.0, 0.5, 0.75])
-    prefill_points("dit_prefill_32k", [0.0, 0.5, 0.7])
-    prefill_points("llama_prefill_16k", [0.0, 0.5, 0.7])
-    decode_points("llama_decode_32k", [0.0, 0.5, 0.7])
-    prefill_points("long_prefill_128k", [0.0, 0.5, 0.7, 0.9])
-    decode_points("long_decode_128k", [0.0, 0.5, 0.7, 0.9])
-    stability()
+    def paged_points():
+        """Paged, ragged decode: 64 sequences of 8K..32K keys in shuffled pages
+        of 128 keys, lambda_b = a / L_b per sequence with the a calibrated for
+        70% on the contiguous 32K cache of the same data; dense and sparse."""
+        from block_sparse_attention_sm_gb300 import capi
+
+        B, Hq, Hkv, d, S, Lmax = 64, 32, 8, 128, 8, 32768
+        rng = np.random.default_rng(7)
+        lens = [int(x) for x in rng.integers(8192, Lmax + 1, size=B)]
+        inp = synth.decode_inputs(B=B, Hq=Hq, Hkv=Hkv, Lk=Lmax, d=d, hot_frac=0.10, seed=0,
+                                  device=dev)
+        q, k, v = inp.q, inp.k, inp.v
+        scale = d ** -0.5
+        a, _ = ss.calibrate("decode", q, k, v, scale=scale, target_sparsity=0.7, num_kv_splits=S)
+        npg = [-(-L // TILE) for L in lens]
+        num_pages, max_pages = sum(npg), max(npg)
+        perm = torch.from_numpy(rng.permutation(num_pages)).to(dev)
+        kp = torch.empty(num_pages, Hkv, TILE, d, dtype=k.dtype, device=dev)
+        vp = torch.empty_like(kp)
+        table = torch.zeros(B, max_pages, dtype=torch.int32, device=dev)
+        off = 0
+        for b, n in enumerate(npg):
+            pg = perm[off:off + n]
+            off += n
+            kp[pg] = k[b, :, :n * TILE].reshape(Hkv, n, TILE, d).permute(1, 0, 2, 3)
+            vp[pg] = v[b, :, :n * TILE].reshape(Hkv, n, TILE, d).permute(1, 0, 2, 3)
+            table[b, :n] = pg.to(torch.int32)
+        del inp, k, v
+        torch.cuda.empty_cache()
+        lens_t = torch.tensor(lens, dtype=torch.int32, device=dev)
+        cnt = torch.zeros(B * Hkv * S, dtype=torch.int32, device=dev)
+        o = torch.empty_like(q)
+        wsn = capi.ss_attn_decode_workspace_size(B, Hq, d, S)
+        ws = torch.empty(wsn, dtype=torch.uint8, device=dev)
+        n_eval = Hkv * num_pages
+        dense_ms = None
+        for tag, aa in (("dense", 0.0), ("a_for_70pct_at_32k", a)):
+            def run():
+                st = capi.ss_attn_decode_paged(q, kp, vp, table, lens_t, o, B, Hq, Hkv, num_pages,
+                                               max_pages, d, scale, aa, S, cnt, ws, wsn)
+                if st != capi.SS_OK:
+                    raise SystemExit(capi.ss_status_string(st))
+            ms = _time_ms(run)
+            sk = int(cnt.sum())
+            kept = n_eval - sk
+            byts = Hkv * sum(lens) * d * 2 + kept * TILE * d * 2 + 2 * B * Hq * d * 2
+            if aa == 0.0:
+                dense_ms = ms
+            emit({"suite": "paged_decode_ragged", "kind": "decode", "point": tag, "a": aa,
+                  "lens": [min(lens), max(lens), sum(lens) // B], "pages": num_pages,
+                  "sparsity": round(sk / n_eval, 4), "ms": round(ms, 4),
+                  "gbs": round(byts / ms / 1e6, 1), "frac_of_peak": round(byts / ms / 1e6 / peaks["hbm"], 4),
+                  "tokens_per_s": round(B / ms * 1e3, 1),
+                  "speedup_vs_dense": round(dense_ms / ms, 3) if dense_ms else None})
+        del q, kp, vp, o
+        torch.cuda.empty_cache()
+
+    parts = set(filter(None, args.suite_only.split(","))) or {"prefill", "decode", "paged", "stability"}
+    if "prefill" in parts:
+        prefill_points("tiny_prefill", [0.0, 0.5, 0.75])
+        prefill_points("dit_prefill_32k", [0.0, 0.5, 0.7])
+        prefill_points("llama_prefill_16k", [0.0, 0.5, 0.7])
+    if "decode" in parts:
+        decode_points("llama_decode_32k", [0.0, 0.5, 0.7])
+    if "prefill" in parts:
+        prefill_points("long_prefill_128k", [0.0, 0.5, 0.7, 0.9])
+    if "decode" in parts:
+        decode_points("long_decode_128k", [0.0, 0.5, 0.7, 0.9])
+    if "paged" in parts:
+        paged_points()
+    if "stability" in parts:
+        stability()
 
 
 def cpu_baseline(q, k, v, cfg, lam, seconds_budget):
@@ -620,6 +685,8 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--suite-only", default="",
+                    help="with --suite: run only the named parts (comma-separated: prefill, decode, paged, stability)")
     ap.add_argument("--suite", action="store_true",
                     help="measure every workload (calibrated sweeps, fits, stability); JSON lines")
     ap.add_argument("--profile", action="store_true",

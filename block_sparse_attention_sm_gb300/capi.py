@@ -19,8 +19,8 @@ SS_PREFILL, SS_DECODE = 0, 1
 
 EXPORTS = (
     "ss_attn_prefill", "ss_attn_prefill_ex", "ss_attn_decode_workspace_size", "ss_attn_decode",
-    "ss_attn_decode_ex", "ss_attn_decode_noalloc", "ss_calibrate", "ss_fit_factor", "ss_lambda", "ss_status_string",
-    "ss_stream_status",
+    "ss_attn_decode_ex", "ss_attn_decode_noalloc", "ss_attn_decode_paged", "ss_calibrate",
+    "ss_fit_factor", "ss_lambda", "ss_status_string", "ss_stream_status",
 )
 
 
@@ -65,6 +65,8 @@ def load() -> ctypes.CDLL:
     lib.ss_attn_decode.argtypes = dec + [P]
     lib.ss_attn_decode_ex.argtypes = dec + [ctypes.POINTER(ss_debug_opts), P]
     lib.ss_attn_decode_noalloc.argtypes = [P, P, P, P, I, I, I, I, I, F, F, I, P, P]
+    lib.ss_attn_decode_paged.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, F, F, I, P, P, U,
+                                         ctypes.POINTER(ss_debug_opts), P]
     lib.ss_attn_decode_workspace_size.argtypes = [I, I, I, I]
     lib.ss_attn_decode_workspace_size.restype = U
     lib.ss_calibrate.argtypes = [ctypes.POINTER(ss_problem), F, ctypes.POINTER(F), ctypes.POINTER(F)]
@@ -76,7 +78,8 @@ def load() -> ctypes.CDLL:
     lib.ss_status_string.restype = ctypes.c_char_p
     lib.ss_stream_status.argtypes = [P]
     for name in ("ss_attn_prefill", "ss_attn_prefill_ex", "ss_attn_decode", "ss_attn_decode_ex",
-                 "ss_attn_decode_noalloc", "ss_calibrate", "ss_fit_factor", "ss_stream_status"):
+                 "ss_attn_decode_noalloc", "ss_attn_decode_paged", "ss_calibrate", "ss_fit_factor",
+                 "ss_stream_status"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -153,6 +156,19 @@ def ss_attn_decode_noalloc(q, k_cache, v_cache, o, B, Hq, Hkv, Lk, d, scale, lam
     return load().ss_attn_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), B, Hq,
                                          Hkv, Lk, d, float(scale), float(lam), int(num_kv_splits),
                                          _ptr(skip_counts), _stream(stream))
+
+
+def ss_attn_decode_paged(q, k_pages, v_pages, page_table, seq_lens, o, B, Hq, Hkv, num_pages,
+                         max_pages, d, scale, lambda_a, num_kv_splits, skip_counts=None,
+                         workspace=None, workspace_bytes=0, skip_mask=None, vote_margin=None,
+                         count_only=False, stream=None) -> int:
+    """Decode over a paged, variable-length KV cache (pages of 128 keys)."""
+    dbg = _dbg(skip_mask, vote_margin, count_only)
+    return load().ss_attn_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table),
+                                       _ptr(seq_lens), _ptr(o), B, Hq, Hkv, num_pages, max_pages,
+                                       d, float(scale), float(lambda_a), int(num_kv_splits),
+                                       _ptr(skip_counts), _ptr(workspace), int(workspace_bytes),
+                                       ctypes.byref(dbg), _stream(stream))
 
 
 SS_DECODE_STATIC_SCRATCH_BYTES = 16 << 20

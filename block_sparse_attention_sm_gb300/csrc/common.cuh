@@ -92,6 +92,15 @@ struct DecodeParams {
   uint32_t* status;
   int count_only;
   int fault_inject;  // test only: skip one K copy per split (bounded-wait expiry)
+  // Paged KV cache (nullptr: contiguous [B][Hkv][Lk][d]).  K and V are pages
+  // of one 128-key tile, [num_pages][Hkv][128][d]; page_table[b][j] is the
+  // page of sequence b's tile j; seq_lens[b] its length.  Each sequence has
+  // its own threshold lambda_b = min(1, lambda_a / seq_len) and its own
+  // split of its ceil(seq_len / 128) tiles.
+  const int32_t* page_table;
+  const int32_t* seq_lens;
+  int max_pages;
+  float lambda_a;
 };
 
 // Launchers (return a CUDA error code; arguments are already validated).

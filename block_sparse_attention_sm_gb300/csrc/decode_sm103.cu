@@ -156,9 +156,28 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   const int split = blockIdx.x % p.S;
   const int bk = blockIdx.x / p.S;  // b * Hkv + kvh
   const int b = bk / p.Hkv, kvh = bk - (bk / p.Hkv) * p.Hkv;
-  const int j0 = split * p.T;
-  const int nt = max(0, min(p.nT, j0 + p.T) - j0);
-  auto tile_rows = [&](int t) { return min(kTile, p.Lk - (j0 + t) * kTile); };
+  // Sequence geometry: one length for the batch, or per sequence (paged).
+  const bool paged = p.page_table != nullptr;
+  int len = p.Lk, nT_b = p.nT, T_b = p.T, row_stride = p.nT;
+  float thr_raw = p.thr_raw;
+  if (paged) {
+    len = max(0, min(p.seq_lens[b], p.max_pages * kTile));
+    nT_b = (len + kTile - 1) / kTile;
+    T_b = (nT_b + p.S - 1) / p.S;
+    row_stride = p.max_pages;
+    // lambda_b = min(1, a / L_b) ("Skip-Softmax" §The threshold); a = 0: dense
+    thr_raw = (p.lambda_a > 0.f && len > 0)
+                  ? logf(fminf(1.f, p.lambda_a / static_cast<float>(len))) / p.scale
+                  : -INFINITY;
+  }
+  const int j0 = split * T_b;
+  const int nt = max(0, min(nT_b, j0 + T_b) - j0);
+  auto tile_rows = [&](int t) { return min(kTile, len - (j0 + t) * kTile); };
+  // Tensor-map coordinates (row, outer) of the split's tile t.
+  auto tile_y = [&](int t) { return paged ? 0 : (j0 + t) * kTile; };
+  auto tile_z = [&](int t) {
+    return paged ? p.page_table[static_cast<long>(b) * p.max_pages + j0 + t] * p.Hkv + kvh : bk;
+  };
 
   // ------------------------------------------------------------------ setup
   int n_k_issued = 0;  // K producer bookkeeping (teardown)
@@ -169,7 +188,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 #pragma unroll
     for (int c = 0; c < C::kChunks; ++c)
       tma_load_3d(sK + st * C::kTileBytes + c * 16384, &tmK, &ctl->k_full[st], c * 64,
-                  (j0 + t) * kTile, bk);
+                  tile_y(t), tile_z(t));
     n_k_issued = t + 1;
   };
   if (warp == kWarpK && lane == 0) {
@@ -250,7 +269,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 #pragma unroll
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_3d(sV + s * C::kTileBytes + c * 16384, &tmV, &ctl->v_full[s], c * 64,
-                        (j0 + t) * kTile, bk);
+                        tile_y(t), tile_z(t));
           n_v_issued = i + 1;
         }
       }
@@ -394,9 +413,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       for (int g = 0; g < GP; ++g)
         if (g < G && tm[g] != -INFINITY)
           cval = fmaxf(cval, (m[g] == -INFINITY) ? INFINITY : tm[g] - m[g]);
-      const bool skip = kVote && cval < p.thr_raw;
+      const bool skip = kVote && cval < thr_raw;
       if (tid == 0) {
-        const long gi = static_cast<long>(bk) * p.nT + j0 + t;
+        const long gi = static_cast<long>(bk) * row_stride + j0 + t;
         if (p.mask != nullptr) p.mask[gi] = skip ? 1 : 0;
         if (p.margin != nullptr) p.margin[gi] = (cval == INFINITY) ? INFINITY : cval * p.scale;
         skipped += skip ? 1u : 0u;
@@ -432,6 +451,20 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           if (g < G)
             *reinterpret_cast<__nv_bfloat16*>(ps + g * 128 + ((j8 ^ (g & 7)) << 4)) =
                 __float2bfloat16_rn(pv);
+        }
+        if (paged && tile_rows(t) < kTile) {
+          // A page's rows past the sequence end hold whatever the cache
+          // holds (TMA fills only rows outside the tensor map with zeros):
+          // zero them so that P = 0 there cannot meet a non-finite V.
+          ok = wwait(&ctl->v_full[sl], (kept / NV) & 1) && ok;
+          if (key >= tile_rows(t)) {
+#pragma unroll
+            for (int c = 0; c < C::kChunks; ++c) {
+              uint4* row = reinterpret_cast<uint4*>(sV + sl * C::kTileBytes + c * 16384 + key * 128);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) row[e] = make_uint4(0u, 0u, 0u, 0u);
+            }
+          }
         }
         float mine_m = 0.f;
 #pragma unroll
@@ -499,6 +532,12 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       }
     }
     if (tid == 0 && p.counts != nullptr) p.counts[static_cast<long>(bk) * p.S + split] = skipped;
+    if (paged && split == 0 && tid < 32)
+      for (int j = nT_b + tid; j < p.max_pages; j += 32) {
+        const long gi = static_cast<long>(bk) * row_stride + j;
+        if (p.mask != nullptr) p.mask[gi] = 2;
+        if (p.margin != nullptr) p.margin[gi] = NAN;
+      }
     tc_fence_before();
     __syncwarp();
   }

@@ -303,6 +303,71 @@ ss_status ss_attn_decode(const void* q, const void* k_cache, const void* v_cache
                            num_kv_splits, skip_counts, workspace, workspace_bytes, nullptr, stream);
 }
 
+ss_status ss_attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                               const int32_t* page_table, const int32_t* seq_lens, void* o,
+                               int B, int Hq, int Hkv, int num_pages, int max_pages, int d,
+                               float scale, float lambda_a, int num_kv_splits,
+                               uint32_t* skip_counts, void* workspace, size_t workspace_bytes,
+                               const ss_debug_opts* dbg, void* stream) {
+  const bool count_only = dbg != nullptr && dbg->count_only != 0;
+  if (q == nullptr || k_pages == nullptr || v_pages == nullptr || page_table == nullptr ||
+      seq_lens == nullptr || (o == nullptr && !count_only))
+    return SS_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) ||
+      (o != nullptr && !aligned16(o)))
+    return SS_ERR_INVALID_ARG;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || num_pages < 1 || max_pages < 1 ||
+      num_kv_splits < 1 || !scale_ok(scale) || !(lambda_a >= 0.f) || !std::isfinite(lambda_a))
+    return SS_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return SS_ERR_UNSUPPORTED;
+  if (Hq / Hkv > 16) return SS_ERR_UNSUPPORTED;
+  const int S = num_kv_splits;
+  if (static_cast<long>(B) * Hkv * S > 0x7fffffffL ||
+      static_cast<long>(num_pages) * Hkv > 0x7fffffffL ||
+      static_cast<long>(B) * max_pages > 0x7fffffffL || static_cast<long>(max_pages) * kTile > 0x7fffffffL)
+    return SS_ERR_INVALID_ARG;
+  if (!count_only && S > 1) {
+    if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < decode_ws(B, Hq, d, S))
+      return SS_ERR_WORKSPACE;
+  }
+  ss_status st = check_device();
+  if (st != SS_OK) return st;
+  CUtensorMap tk, tv;
+  const long pages_x_heads = static_cast<long>(num_pages) * Hkv;
+  if (!make_map(&tk, k_pages, d, kTile, pages_x_heads) || !make_map(&tv, v_pages, d, kTile, pages_x_heads))
+    return SS_ERR_CUDA;
+
+  DecodeParams p{};
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Lk = 0;  // per sequence
+  p.d = d;
+  p.G = Hq / Hkv;
+  p.nT = max_pages;
+  p.S = S;
+  p.T = 0;
+  p.scale = scale;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.thr_raw = -INFINITY;  // per sequence from lambda_a
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.part = static_cast<float*>(workspace);
+  p.counts = skip_counts;
+  p.mask = dbg ? dbg->skip_mask : nullptr;
+  p.margin = dbg ? dbg->vote_margin : nullptr;
+  p.status = status_ptr();
+  p.count_only = count_only ? 1 : 0;
+  p.fault_inject = 0;
+  p.page_table = page_table;
+  p.seq_lens = seq_lens;
+  p.max_pages = max_pages;
+  p.lambda_a = lambda_a;
+  const Mode mode = count_only ? Mode::kCount : (lambda_a == 0.f ? Mode::kDense : Mode::kSparse);
+  cudaError_t e = launch_decode(tk, tv, p, mode, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+}
+
 ss_status ss_attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
                                  void* o, int B, int Hq, int Hkv, int Lk, int d, float scale,
                                  float lambda, int num_kv_splits, uint32_t* skip_counts,

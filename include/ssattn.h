@@ -147,6 +147,40 @@ ss_status ss_attn_decode_ex(const void* q, const void* k_cache, const void* v_ca
                             size_t workspace_bytes, const ss_debug_opts* dbg, void* stream);
 
 /*
+ * Split-KV decode over a paged, variable-length KV cache (the serving
+ * layout the pages' engine integrations imply: BLASST summary,
+ * §Belangrijkste Bijdragen -- TensorRT-LLM / FlashInfer; the skip test per
+ * sequence follows "Skip-Softmax" §The threshold).
+ *   k_pages, v_pages: bf16 [num_pages][Hkv][128][d], 16-byte aligned; a page
+ *     holds one 128-key tile of one sequence for every KV head.
+ *   page_table: device int32 [B][max_pages]; entry j of row b is the page of
+ *     sequence b's keys [128j, 128j + 128).  Entries past a sequence's last
+ *     page are not read.  An entry outside [0, num_pages) reads zeros.
+ *   seq_lens: device int32 [B], keys per sequence (0 .. 128*max_pages; larger
+ *     values are clamped).  The rows of a sequence's last page past its end
+ *     are ignored, whatever they hold.
+ *   lambda_a: the a of lambda = a / L, applied per sequence with L its own
+ *     length: lambda_b = min(1, lambda_a / seq_lens[b]); 0 keeps every tile.
+ *   num_kv_splits: each sequence's ceil(L_b/128) tiles are cut into this
+ *     many contiguous ranges of ceil(tiles_b / num_kv_splits) tiles (ranges
+ *     past the end are empty).
+ *   skip_counts: nullable, [B*Hkv*num_kv_splits] as in ss_attn_decode.
+ *   workspace: as in ss_attn_decode (ss_attn_decode_workspace_size).
+ *   dbg: nullable; skip_mask / vote_margin are [B*Hkv][max_pages] (tiles past
+ *     a sequence's end are marked not evaluated); count_only as elsewhere.
+ * Returns SS_OK, SS_ERR_INVALID_ARG (null pointer, misalignment, B, Hq, Hkv,
+ * num_pages, max_pages or num_kv_splits < 1, Hq % Hkv != 0, scale <= 0,
+ * lambda_a < 0 or not finite), SS_ERR_UNSUPPORTED, SS_ERR_WORKSPACE or
+ * SS_ERR_CUDA.
+ */
+ss_status ss_attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
+                               const int32_t* page_table, const int32_t* seq_lens, void* o,
+                               int B, int Hq, int Hkv, int num_pages, int max_pages, int d,
+                               float scale, float lambda_a, int num_kv_splits,
+                               uint32_t* skip_counts, void* workspace, size_t workspace_bytes,
+                               const ss_debug_opts* dbg, void* stream);
+
+/*
  * Decode for callers that cannot allocate device memory.  The pages have no
  * counterpart to this entry point; it exists for users of this library, not
  * for the method.

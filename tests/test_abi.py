@@ -104,6 +104,29 @@ def test_decode_rejects_before_launch(capi, kw, expect):
     assert st == getattr(capi, expect)
 
 
+@pytest.mark.parametrize("kw,expect", [
+    (dict(table=None), "SS_ERR_INVALID_ARG"),
+    (dict(lens=None), "SS_ERR_INVALID_ARG"),
+    (dict(num_pages=0), "SS_ERR_INVALID_ARG"),
+    (dict(max_pages=0), "SS_ERR_INVALID_ARG"),
+    (dict(a=-1.0), "SS_ERR_INVALID_ARG"),
+    (dict(a=float("inf")), "SS_ERR_INVALID_ARG"),
+    (dict(k=FAKE + 4), "SS_ERR_INVALID_ARG"),
+    (dict(d=96), "SS_ERR_UNSUPPORTED"),
+    (dict(Hq=64, Hkv=2), "SS_ERR_UNSUPPORTED"),
+    (dict(S=4, ws=None), "SS_ERR_WORKSPACE"),
+])
+def test_paged_decode_rejects_before_launch(capi, kw, expect):
+    args = dict(k=FAKE, table=FAKE, lens=FAKE, B=2, Hq=8, Hkv=2, num_pages=10, max_pages=4, d=128,
+                a=1.0, S=1, ws=FAKE, ws_bytes=1 << 30)
+    args.update(kw)
+    st = capi.ss_attn_decode_paged(FAKE, args["k"], FAKE, args["table"], args["lens"], FAKE,
+                                   args["B"], args["Hq"], args["Hkv"], args["num_pages"],
+                                   args["max_pages"], args["d"], 0.1, args["a"], args["S"], None,
+                                   args["ws"], args["ws_bytes"], stream=0)
+    assert st == getattr(capi, expect)
+
+
 def test_struct_layouts_match_the_header(capi, tmp_path):
     """ctypes mirrors of the C structs have the C compiler's sizes and offsets."""
     src = tmp_path / "sz.c"
