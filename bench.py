@@ -558,11 +558,14 @@ def run_suite(args):
         del q, kp, vp, o
         torch.cuda.empty_cache()
 
-    parts = set(filter(None, args.suite_only.split(","))) or {"prefill", "decode", "paged", "stability"}
+    parts = set(filter(None, args.suite_only.split(","))) or {"prefill", "chunked", "decode", "paged",
+                                                                  "stability"}
     if "prefill" in parts:
         prefill_points("tiny_prefill", [0.0, 0.5, 0.75])
         prefill_points("dit_prefill_32k", [0.0, 0.5, 0.7])
         prefill_points("llama_prefill_16k", [0.0, 0.5, 0.7])
+    if "chunked" in parts:
+        prefill_points("llama_chunked_prefill_2k_on_32k", [0.0, 0.5, 0.7, 0.9])
     if "decode" in parts:
         decode_points("llama_decode_32k", [0.0, 0.5, 0.7])
     if "prefill" in parts:
@@ -686,7 +689,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--suite-only", default="",
-                    help="with --suite: run only the named parts (comma-separated: prefill, decode, paged, stability)")
+                    help="with --suite: run only the named parts (comma-separated: prefill, chunked, decode, paged, stability)")
     ap.add_argument("--suite", action="store_true",
                     help="measure every workload (calibrated sweeps, fits, stability); JSON lines")
     ap.add_argument("--profile", action="store_true",

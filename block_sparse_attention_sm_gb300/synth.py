@@ -128,6 +128,12 @@ WORKLOADS = {
                               causal=True, scale=128 ** -0.5, hot_frac=0.10, per_head_u=True),
     "llama_decode_32k": dict(kind="decode", B=64, Hq=32, Hkv=8, Lk=32768, d=128,
                              scale=128 ** -0.5, hot_frac=0.10, per_head_u=True, num_splits=8),
+    # chunked prefill: 2048 new tokens of each of 4 sequences against a 32K
+    # cache (keys of the earlier chunks plus the new ones), causal from the
+    # bottom-right
+    "llama_chunked_prefill_2k_on_32k": dict(kind="prefill", B=4, Hq=32, Hkv=8, Lq=2048,
+                                            Lk=32768, d=128, causal=True, scale=128 ** -0.5,
+                                            hot_frac=0.10, per_head_u=True),
     "long_prefill_128k": dict(kind="prefill", B=1, Hq=32, Hkv=8, Lq=131072, Lk=131072, d=128,
                               causal=True, scale=128 ** -0.5, hot_frac=0.05, per_head_u=True),
     "long_decode_128k": dict(kind="decode", B=8, Hq=32, Hkv=8, Lk=131072, d=128,

@@ -75,6 +75,29 @@ def test_multi_run_votes(shape, a):
                   lam=min(1.0, a / Lk), chunk=chunk)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_long_gap_between_kept_tiles(d):
+    """One CTA's two query blocks keep disjoint tiles: block 0 only the first
+    and the last of 32, block 1 the 30 between.  Block 0's next K then sits
+    far past its last V in the shared ring of copies, so it must not wait for
+    that copy while still holding the V (regression case for that wait)."""
+    from _parity import check_prefill
+
+    g = torch.Generator(device="cuda").manual_seed(9)
+    Lq, Lk = 256, 32 * 128
+    e1 = torch.zeros(d, device="cuda")
+    e2 = torch.zeros(d, device="cuda")
+    e1[0], e2[1] = 1.0, 1.0
+    noise = lambda n: 0.05 * torch.randn(n, d, device="cuda", generator=g)
+    q = torch.cat([16 * e1 + noise(128), 16 * e2 + noise(128)])
+    k = 16 * e2.expand(Lk, d) + noise(Lk)
+    k[:128] = 16 * e1 + noise(128)
+    k[-128:] = 16 * e1 + noise(128)
+    v = torch.randn(Lk, d, device="cuda", generator=g)
+    q, k, v = (t.reshape(1, 1, -1, d).to(torch.bfloat16) for t in (q, k, v))
+    check_prefill(q, k, v, scale=d ** -0.5, causal=False, lam=1e-3)
+
+
 def test_random_scores_many_decisions():
     """Plain N(0,1) inputs (no planted structure): margins spread out, so many
     tiles sit near the threshold -- exercises the near-margin accounting."""
@@ -97,7 +120,8 @@ def _sampled_units(B, Hq, nqb, heads, rng):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("workload,a", [("dit_prefill_32k", 3.0), ("llama_prefill_16k", 2.0)])
+@pytest.mark.parametrize("workload,a", [("dit_prefill_32k", 3.0), ("llama_prefill_16k", 2.0),
+                                        ("llama_chunked_prefill_2k_on_32k", 2.0)])
 def test_full_size_sampled(workload, a):
     """Full-size workloads in the bench's launch configuration; the oracle
     checks sampled query blocks (first, last, random) of a few heads."""
