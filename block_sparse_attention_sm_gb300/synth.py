@@ -117,6 +117,39 @@ def decode_inputs(*, B, Hq, Hkv, Lk, d, hot_frac, seed=0, per_head_u=True, devic
     return Inputs(q, k, v, hot, u)
 
 
+@dataclass
+class MlaInputs:
+    q: torch.Tensor          # [B,Hq,dk] bf16, dk = d_latent + d_rope
+    kv: torch.Tensor         # [B,Lk,dk] bf16: latent part, then rotary part
+    hot: np.ndarray          # [B,1,nT] bool
+    u: np.ndarray            # [1,dk] fp64
+
+
+def mla_decode_inputs(*, B, Hq, Lk, d_latent=512, d_rope=64, hot_frac, seed=0, device="cpu",
+                      shift=HOT_SHIFT) -> MlaInputs:
+    """Latent-attention decode: q [B,Hq,dk] and one latent cache kv [B,Lk,dk]
+    shared by all heads; the same hot-tile structure over the full key width
+    (the values are the latent part of the same rows)."""
+    dk = d_latent + d_rope
+    nT = -(-Lk // TILE)
+    hot = hot_tiles(seed, B, 1, nT, hot_frac)
+    u = directions(seed, 1, dk, False)
+    ut = torch.as_tensor(u[0], dtype=torch.float32, device=device)
+    q = _randn((B, Hq, dk), seed * 100003, 3, device)
+    q += shift * ut
+    q = q.to(torch.bfloat16)
+    kv = torch.empty((B, Lk, dk), dtype=torch.bfloat16, device=device)
+    for b in range(B):
+        kb = _randn((Lk, dk), seed * 100003 + b, 4, device)
+        tiles = np.nonzero(hot[b, 0])[0]
+        rows = (tiles[:, None] * TILE + np.arange(TILE)[None, :]).ravel()
+        rows = rows[rows < Lk]
+        kb.index_add_(0, torch.as_tensor(rows, device=device), (shift * ut).expand(len(rows), dk))
+        kv[b] = kb.to(torch.bfloat16)
+        del kb
+    return MlaInputs(q, kv, hot, u)
+
+
 # The workloads, by what they are (shapes from the method's two target uses:
 # video-DiT self-attention and Llama-3.1-8B-style GQA prefill/decode).
 WORKLOADS = {
@@ -134,6 +167,11 @@ WORKLOADS = {
     "llama_chunked_prefill_2k_on_32k": dict(kind="prefill", B=4, Hq=32, Hkv=8, Lq=2048,
                                             Lk=32768, d=128, causal=True, scale=128 ** -0.5,
                                             hot_frac=0.10, per_head_u=True),
+    # latent-attention decode (absorbed form): 16 query heads sharing one
+    # latent head of 512 + 64 rotary dims (DeepSeek-V2-Lite's heads, or
+    # DeepSeek-V3's 128 over 8 GPUs); softmax scale 1/sqrt(128 + 64)
+    "mla_decode_32k": dict(kind="mla_decode", B=64, Hq=16, Lk=32768, d_latent=512, d_rope=64,
+                           scale=192 ** -0.5, hot_frac=0.10, num_splits=16),
     "long_prefill_128k": dict(kind="prefill", B=1, Hq=32, Hkv=8, Lq=131072, Lk=131072, d=128,
                               causal=True, scale=128 ** -0.5, hot_frac=0.05, per_head_u=True),
     "long_decode_128k": dict(kind="decode", B=8, Hq=32, Hkv=8, Lk=131072, d=128,
@@ -145,7 +183,11 @@ def make(workload: str, seed: int = 0, device="cpu", **overrides) -> tuple[Input
     """Inputs for a named workload (shape fields may be overridden)."""
     cfg = dict(WORKLOADS[workload])
     cfg.update(overrides)
-    if cfg["kind"] == "prefill":
+    if cfg["kind"] == "mla_decode":
+        inp = mla_decode_inputs(B=cfg["B"], Hq=cfg["Hq"], Lk=cfg["Lk"], d_latent=cfg["d_latent"],
+                                d_rope=cfg["d_rope"], hot_frac=cfg["hot_frac"], seed=seed,
+                                device=device)
+    elif cfg["kind"] == "prefill":
         inp = prefill_inputs(B=cfg["B"], Hq=cfg["Hq"], Hkv=cfg["Hkv"], Lq=cfg["Lq"], Lk=cfg["Lk"],
                              d=cfg["d"], hot_frac=cfg["hot_frac"], seed=seed,
                              per_head_u=cfg["per_head_u"], device=device)

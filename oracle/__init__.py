@@ -52,6 +52,7 @@ class _Decode(ctypes.Structure):
         ("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int),
         ("Lk", ctypes.c_int), ("d", ctypes.c_int), ("scale", ctypes.c_double),
         ("lam", ctypes.c_double), ("num_splits", ctypes.c_int), ("Bk", ctypes.c_int),
+        ("dv", ctypes.c_int),
     ]
 
 
@@ -105,13 +106,13 @@ class PrefillResult:
 
 @dataclass
 class DecodeResult:
-    o: np.ndarray        # [n, G, d]
+    o: np.ndarray        # [n, G, dv]
     mask: np.ndarray     # [n, nT]
     margin: np.ndarray   # [n, nT]
     counts: np.ndarray   # [n, S]
     part_m: np.ndarray   # [n, G, S]
     part_l: np.ndarray   # [n, G, S]
-    part_o: np.ndarray   # [n, G, S, d]
+    part_o: np.ndarray   # [n, G, S, dv]
     units: np.ndarray
 
 
@@ -144,10 +145,14 @@ def prefill(q, k, v, *, scale: float, causal: bool, lam: float, Bq: int = 128, B
 
 def decode(q, k, v, *, scale: float, lam: float, num_splits: int, Bk: int = 128, units=None,
            mask_override=None) -> DecodeResult:
-    """Skip-softmax split-KV decode over q [B,Hq,d], k/v [B,Hkv,Lk,d] (bf16)."""
+    """Skip-softmax split-KV decode over q [B,Hq,d], k [B,Hkv,Lk,d] and
+    v [B,Hkv,Lk,dv] (bf16; dv may differ from d)."""
     qb, kb, vb = _bits(q), _bits(k), _bits(v)
     B, Hq, d = qb.shape
-    _, Hkv, Lk, _ = kb.shape
+    _, Hkv, Lk, dk = kb.shape
+    dv = vb.shape[-1]
+    if dk != d or vb.shape[:3] != kb.shape[:3]:
+        raise ValueError("decode: q/k widths or k/v shapes disagree")
     G = Hq // Hkv
     S = int(num_splits)
     nT = -(-Lk // Bk)
@@ -155,23 +160,44 @@ def decode(q, k, v, *, scale: float, lam: float, num_splits: int, Bk: int = 128,
         units = np.arange(B * Hkv, dtype=np.int64)
     units = np.ascontiguousarray(np.asarray(units, dtype=np.int64))
     n = len(units)
-    o = np.zeros((n, G, d), np.float64)
+    o = np.zeros((n, G, dv), np.float64)
     mask = np.zeros((n, nT), np.uint8)
     margin = np.zeros((n, nT), np.float64)
     counts = np.zeros((n, S), np.uint32)
     pm = np.zeros((n, G, S), np.float64)
     pl = np.zeros((n, G, S), np.float64)
-    po = np.zeros((n, G, S, d), np.float64)
+    po = np.zeros((n, G, S, dv), np.float64)
     ov = None
     if mask_override is not None:
         ov = np.ascontiguousarray(np.asarray(mask_override, dtype=np.uint8).reshape(n, nT))
-    prob = _Decode(B, Hq, Hkv, Lk, d, float(scale), float(lam), S, Bk)
+    prob = _Decode(B, Hq, Hkv, Lk, d, float(scale), float(lam), S, Bk, dv)
     rc = _get().orc_decode(ctypes.byref(prob), _ptr(qb), _ptr(kb), _ptr(vb), _ptr(units), n,
                            _ptr(ov), _ptr(o), _ptr(mask), _ptr(margin), _ptr(counts),
                            _ptr(pm), _ptr(pl), _ptr(po))
     if rc != 0:
         raise ValueError("orc_decode rejected its arguments")
     return DecodeResult(o, mask, margin, counts, pm, pl, po, units)
+
+
+def mla_decode(q, kv, *, d_latent: int, scale: float, lam: float, num_splits: int,
+               Bk: int = 128, units=None, mask_override=None) -> DecodeResult:
+    """Decode with multi-head latent attention over q [B,Hq,dk] and one
+    latent cache kv [B,Lk,dk] (bf16) shared by every query head.
+
+    Reading of the pages' "MLA" (the "Skip-Softmax" design doc lists it among
+    the supported attention kinds without giving its shapes): the absorbed
+    form, in which the keys are the cache rows (latent part followed by the
+    rotary part, dk wide) and the values are their first d_latent entries.
+    All Hq heads share the one latent head, so they form the voting group.
+    This is `decode` with Hkv = 1, k = kv and v = kv[..., :d_latent] (a copy
+    of the inputs, no arithmetic)."""
+    kb = _bits(kv)
+    if kb.ndim != 3 or not 0 < d_latent <= kb.shape[-1]:
+        raise ValueError("mla_decode: kv must be [B, Lk, dk] with d_latent <= dk")
+    k = kb[:, None]
+    v = np.ascontiguousarray(kb[:, None, :, :d_latent])
+    return decode(q, k, v, scale=scale, lam=lam, num_splits=num_splits, Bk=Bk, units=units,
+                  mask_override=mask_override)
 
 
 def calibrate(margin: np.ndarray, mask: np.ndarray, target: float, L: float):

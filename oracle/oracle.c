@@ -53,13 +53,14 @@ static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 /*
  * The per-row running state of the online pass and one tile of it.
  *
- * `rows` query rows (pointers into q, each d long), keys [k0, k0 + nk) of one
- * head (pointers kh, vh to row 0 of that head).  visible(r, key) is given by
- * `last_visible[r]`: keys with index > last_visible[r] are masked.
+ * `rows` query rows (pointers into q, each dk long), keys [k0, k0 + nk) of one
+ * head (pointers kh, vh to row 0 of that head; key rows are dk long, value
+ * rows d = st->d long).  visible(r, key) is given by `last_visible[r]`: keys
+ * with index > last_visible[r] are masked.
  * Returns ORC_KEPT / ORC_SKIPPED / ORC_NOT_EVALUATED and writes c_j.
  */
 typedef struct {
-  int rows, d;
+  int rows, d; /* d: value width (columns of O) */
   double* m; /* [rows] */
   double* l; /* [rows] */
   double* O; /* [rows][d] */
@@ -74,7 +75,7 @@ static void state_reset(run_state* st) {
 }
 
 static int tile_step(run_state* st, const uint16_t* const* qrows, const int64_t* last_visible,
-                     const uint16_t* kh, const uint16_t* vh, int64_t k0, int64_t nk,
+                     const uint16_t* kh, int dk, const uint16_t* vh, int64_t k0, int64_t nk,
                      double scale, double ln_lambda, int have_override, int override_skip,
                      double* s /* scratch [rows][nk] */, double* tmax /* scratch [rows] */,
                      double* c_out) {
@@ -86,7 +87,7 @@ static int tile_step(run_state* st, const uint16_t* const* qrows, const int64_t*
     for (int64_t t = 0; t < nk; ++t) {
       const int64_t key = k0 + t;
       double x = -INFINITY;
-      if (key <= last_visible[r]) x = scale * dot_bf16(qrows[r], kh + (size_t)key * d, d);
+      if (key <= last_visible[r]) x = scale * dot_bf16(qrows[r], kh + (size_t)key * dk, dk);
       s[(size_t)r * nk + t] = x;
       if (x > tmax[r]) tmax[r] = x;
     }
@@ -182,7 +183,7 @@ int orc_prefill(const orc_prefill_problem* p, const uint16_t* q, const uint16_t*
       const int ov = have_ov ? mask_override[(size_t)i * nT + j] : 0;
       double c;
       const int dec =
-          tile_step(&st, qrows, last_vis, kh, vh, k0, nk, p->scale, ln_lambda, have_ov, ov, s, tmax, &c);
+          tile_step(&st, qrows, last_vis, kh, d, vh, k0, nk, p->scale, ln_lambda, have_ov, ov, s, tmax, &c);
       if (dec == ORC_SKIPPED) ++skipped;
       if (mask) mask[(size_t)i * nT + j] = (uint8_t)dec;
       if (margin) margin[(size_t)i * nT + j] = c;
@@ -209,9 +210,11 @@ int orc_decode(const orc_decode_problem* p, const uint16_t* q, const uint16_t* k
                uint32_t* counts, double* part_m, double* part_l, double* part_o) {
   if (!p || !q || !k || !v) return -1;
   if (p->B < 1 || p->Hq < 1 || p->Hkv < 1 || p->Hq % p->Hkv != 0 || p->Lk < 1 || p->d < 1 ||
-      p->Bk < 1 || p->num_splits < 1 || !(p->lambda >= 0.0) || p->lambda > 1.0)
+      p->dv < 0 || p->Bk < 1 || p->num_splits < 1 || !(p->lambda >= 0.0) || p->lambda > 1.0)
     return -1;
-  const int G = p->Hq / p->Hkv, d = p->d, Bk = p->Bk, S = p->num_splits;
+  /* dk: query/key width; d: value width (the MLA reading gives them apart) */
+  const int G = p->Hq / p->Hkv, dk = p->d, d = (p->dv > 0) ? p->dv : p->d, Bk = p->Bk,
+            S = p->num_splits;
   const int64_t nT = ceil_div(p->Lk, Bk), T = ceil_div(nT, S);
   const int64_t total = (int64_t)p->B * p->Hkv;
   if (units == NULL) n_units = total;
@@ -237,10 +240,10 @@ int orc_decode(const orc_decode_problem* p, const uint16_t* q, const uint16_t* k
     double* s = st.O + (size_t)G * d;
     double* tmax = s + (size_t)G * Bk;
     for (int g = 0; g < G; ++g) {
-      qrows[g] = q + ((size_t)b * p->Hq + (size_t)kvh * G + g) * d;
+      qrows[g] = q + ((size_t)b * p->Hq + (size_t)kvh * G + g) * dk;
       last_vis[g] = p->Lk - 1;
     }
-    const uint16_t* kh = k + (size_t)(b * p->Hkv + kvh) * p->Lk * d;
+    const uint16_t* kh = k + (size_t)(b * p->Hkv + kvh) * p->Lk * dk;
     const uint16_t* vh = v + (size_t)(b * p->Hkv + kvh) * p->Lk * d;
 
     for (int sp = 0; sp < S; ++sp) {
@@ -254,7 +257,7 @@ int orc_decode(const orc_decode_problem* p, const uint16_t* q, const uint16_t* k
         const int have_ov = mask_override != NULL;
         const int ov = have_ov ? mask_override[(size_t)i * nT + j] : 0;
         double c;
-        const int dec = tile_step(&st, qrows, last_vis, kh, vh, k0, nk, p->scale, ln_lambda,
+        const int dec = tile_step(&st, qrows, last_vis, kh, dk, vh, k0, nk, p->scale, ln_lambda,
                                   have_ov, ov, s, tmax, &c);
         if (dec == ORC_SKIPPED) ++skipped;
         if (mask) mask[(size_t)i * nT + j] = (uint8_t)dec;

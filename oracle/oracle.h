@@ -64,21 +64,24 @@ int orc_prefill(const orc_prefill_problem* p, const uint16_t* q, const uint16_t*
                 uint32_t* counts);
 
 typedef struct {
-  int B, Hq, Hkv, Lk, d;
+  int B, Hq, Hkv, Lk, d; /* d: width of q and k rows */
   double scale;
   double lambda;
   int num_splits; /* contiguous ranges of T = ceil(nT/S) tiles */
   int Bk;
+  int dv;         /* width of v rows and of o; 0: the same as d */
 } orc_decode_problem;
 
 /*
  * Decode (one query token per sequence).  A unit is one (b, kv head) with
  * its G = Hq/Hkv query heads; unit id u = b*Hkv + kvh.  Packed outputs:
- *   o      [n][G][d]
+ * q is [B][Hq][d], k [B][Hkv][Lk][d], v [B][Hkv][Lk][dv] (dv = d unless set:
+ * multi-head latent attention reads values of another width than keys).
+ *   o      [n][G][dv]
  *   mask   [n][nT]   (tiles indexed globally; splits partition them)
  *   margin [n][nT]
  *   counts [n][S]    skipped tiles per split
- *   part_m, part_l [n][G][S], part_o [n][G][S][d]: per-split running state
+ *   part_m, part_l [n][G][S], part_o [n][G][S][dv]: per-split running state
  *          (m in natural-log units, -INF for an empty split), nullable.
  */
 int orc_decode(const orc_decode_problem* p, const uint16_t* q, const uint16_t* k,

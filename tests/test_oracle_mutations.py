@@ -23,6 +23,9 @@ MUTATIONS = {
     "merge_weight_sign": ("exp(sm[(size_t)g * S + sp] - mstar)", "exp(mstar - sm[(size_t)g * S + sp])"),
     "split_floor": ("T = ceil_div(nT, S)", "T = (nT / S > 0 ? nT / S : 1)"),
     "calib_edge": ("a = L * exp(0.5 * (lo + hi));", "a = L * exp(lo);"),
+    "value_head_stride_key_width": ("* p->Lk * dk;\n    const uint16_t* vh = v + (size_t)(b * p->Hkv + kvh) * p->Lk * d;",
+                                    "* p->Lk * dk;\n    const uint16_t* vh = v + (size_t)(b * p->Hkv + kvh) * p->Lk * dk;"),
+    "value_row_stride_key_width": ("vh + (size_t)(k0 + t) * d;", "vh + (size_t)(k0 + t) * dk;"),
     "v_transposed": ("p * bf16_to_double(vk[e])", "p * bf16_to_double(vh[(size_t)e * d + (k0 + t) % d])"),
 }
 

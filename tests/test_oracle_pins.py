@@ -319,6 +319,69 @@ def test_decode_sparse_decisions_and_output(oracle_lib, shape, lam):
         np.testing.assert_allclose(res.o[i], ref, rtol=0, atol=1e-10)
 
 
+# ----------------------------------------------- latent-attention decode pins
+MLA_SHAPES = [
+    # B, Hq, Lk, dk (latent + rotary), d_latent, S, Bk
+    (2, 4, 37, 12, 8, 1, 4),
+    (1, 3, 50, 9, 6, 4, 5),
+    (3, 5, 9, 7, 4, 8, 4),          # more splits than tiles
+    (2, 16, 260, 576, 512, 2, 128),  # the kernel's widths, a ragged last tile
+]
+
+
+def mla_case(oracle_lib, shape, lam, seed):
+    B, Hq, Lk, dk, dl, S, Bk = shape
+    rng = np.random.default_rng(seed)
+    u = rng.standard_normal(dk)
+    u /= np.linalg.norm(u)
+    q = rand_bits(rng, (B, Hq, dk), shift=3.0 * u)
+    kx = rng.standard_normal((B, Lk, dk))
+    kx[rng.random((B, Lk)) < 0.15] += 3.0 * u
+    kv = bf16_bits(kx)
+    scale = 1.0 / math.sqrt(dk)
+    res = oracle_lib.mla_decode(q, kv, d_latent=dl, scale=scale, lam=lam, num_splits=S, Bk=Bk)
+    return (q, kv, scale), res
+
+
+@pytest.mark.parametrize("shape", MLA_SHAPES)
+def test_mla_dense_equals_two_pass_over_latent_values(oracle_lib, shape):
+    """lambda = 0: every head's output is softmax(scale q kv^T) kv[:, :d_latent]
+    (values are the leading latent entries of the same rows), for any split."""
+    B, Hq, Lk, dk, dl, S, Bk = shape
+    (q, kv, scale), res = mla_case(oracle_lib, shape, 0.0, 11)
+    assert res.o.shape == (B, Hq, dl)
+    for b in range(B):
+        kk = f64(kv[b])
+        ref = two_pass(f64(q[b]), kk, kk[:, :dl], scale, np.ones((Hq, Lk), bool))
+        np.testing.assert_allclose(res.o[b], ref, rtol=0, atol=1e-10)
+    for S2 in (1, 3, 7):
+        _, r2 = mla_case(oracle_lib, (B, Hq, Lk, dk, dl, S2, Bk), 0.0, 11)
+        np.testing.assert_allclose(r2.o, res.o, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("shape", MLA_SHAPES)
+@pytest.mark.parametrize("lam", [0.05, 1.0])
+def test_mla_sparse_decisions_and_output(oracle_lib, shape, lam):
+    """All Hq heads vote together; decisions follow the prefix-maximum form
+    over the full key width and the output is the softmax over the kept
+    tiles' keys with latent values."""
+    B, Hq, Lk, dk, dl, S, Bk = shape
+    nT = -(-Lk // Bk)
+    T = -(-nT // S)
+    (q, kv, scale), res = mla_case(oracle_lib, shape, lam, 12)
+    for b in range(B):
+        qq, kk = f64(q[b]), f64(kv[b])
+        s = scale * (qq @ kk.T)
+        for sp in range(S):
+            tiles = list(range(sp * T, min(nT, (sp + 1) * T)))
+            m_ref, c_ref = prefix_decisions(s, Bk, tiles, math.log(lam))
+            np.testing.assert_array_equal(res.mask[b, tiles], m_ref)
+            assert res.counts[b, sp] == (m_ref == 1).sum()
+        keep = np.repeat(res.mask[b] == 0, Bk)[:Lk]
+        ref = two_pass(qq, kk, kk[:, :dl], scale, np.broadcast_to(keep, (Hq, Lk)))
+        np.testing.assert_allclose(res.o[b], ref, rtol=0, atol=1e-10)
+
+
 # ------------------------------------------------------ worked examples
 def _decode_scalar(vals):
     return np.array([math.inf if x == "inf" else x for x in vals], dtype=np.float64)
