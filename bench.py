@@ -501,6 +501,51 @@ def run_suite(args):
         del res
         torch.cuda.empty_cache()
 
+    def mla_points(name, targets):
+        """Latent-attention decode: the cache is read once (the values are its
+        latent part, already on chip); bytes = cache + q + o."""
+        inp, cfg = synth.make(name, seed=0, device=dev,
+                              **({"B": args.mla_batch} if args.mla_batch else {}))
+        q, kv = inp.q, inp.kv
+        B, Hq, dk = q.shape
+        Lk = kv.shape[1]
+        S = cfg["num_splits"]
+        nT = -(-Lk // TILE)
+        cnt = torch.zeros(B * S, dtype=torch.int32, device=dev)
+        o = torch.empty(B, Hq, cfg["d_latent"], dtype=q.dtype, device=dev)
+        wsb, _ = ss.mla_workspace(B, Hq, S, dev)
+        n_eval = B * nT
+        byts = B * Lk * dk * 2 + B * Hq * (dk + cfg["d_latent"]) * 2
+        flops_tile = 2.0 * TILE * Hq * dk  # scores of one tile; P.V adds 2*128*Hq*512 if kept
+        fit_s, fit_a, dense_ms = [], [], None
+        for s_t in targets:
+            a = 0.0
+            if s_t > 0:
+                a, _ = ss.calibrate("mla_decode", q, kv, None, scale=cfg["scale"],
+                                    target_sparsity=s_t, num_kv_splits=S)
+            lam = min(1.0, a / Lk)
+            ms = _time_ms(lambda: ss.mla_decode(q, kv, scale=cfg["scale"], lam=lam, num_kv_splits=S,
+                                                counts=cnt, out=o, workspace=wsb))
+            sk = int(cnt.sum())
+            kept = n_eval - sk
+            if s_t == 0:
+                dense_ms = ms
+            if s_t > 0 and a > 0:
+                fit_s.append(sk / n_eval)
+                fit_a.append(a)
+            flops = flops_tile * n_eval + 2.0 * TILE * Hq * cfg["d_latent"] * kept
+            emit({"suite": name, "kind": "mla_decode", "target": s_t, "a": a, "lambda": lam,
+                  "sparsity": round(sk / n_eval, 4), "ms": round(ms, 4),
+                  "gbs": round(byts / ms / 1e6, 1), "frac_of_peak": round(byts / ms / 1e6 / peaks["hbm"], 4),
+                  "tflops_executed": round(flops / ms / 1e9, 1),
+                  "tokens_per_s": round(B / ms * 1e3, 1),
+                  "speedup_vs_dense": round(dense_ms / ms, 3) if dense_ms else None})
+        if len(fit_s) >= 2:
+            A, Bc = ss.fit_factor(fit_s, fit_a)
+            emit({"suite": name, "kind": "fit", "A": A, "B": Bc, "points": list(zip(fit_s, fit_a))})
+        del q, kv, o, inp
+        torch.cuda.empty_cache()
+
     def paged_points():
         """Paged, ragged decode: 64 sequences of 8K..32K keys in shuffled pages
         of 128 keys, lambda_b = a / L_b per sequence with the a calibrated for
@@ -559,7 +604,7 @@ def run_suite(args):
         torch.cuda.empty_cache()
 
     parts = set(filter(None, args.suite_only.split(","))) or {"prefill", "chunked", "decode", "paged",
-                                                                  "stability"}
+                                                                  "mla", "stability"}
     if "prefill" in parts:
         prefill_points("tiny_prefill", [0.0, 0.5, 0.75])
         prefill_points("dit_prefill_32k", [0.0, 0.5, 0.7])
@@ -574,6 +619,8 @@ def run_suite(args):
         decode_points("long_decode_128k", [0.0, 0.5, 0.7, 0.9])
     if "paged" in parts:
         paged_points()
+    if "mla" in parts:
+        mla_points("mla_decode_32k", [0.0, 0.5, 0.7, 0.9])
     if "stability" in parts:
         stability()
 
@@ -689,7 +736,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--suite-only", default="",
-                    help="with --suite: run only the named parts (comma-separated: prefill, chunked, decode, paged, stability)")
+                    help="with --suite: run only the named parts (comma-separated: prefill, chunked, decode, paged, mla, stability)")
     ap.add_argument("--suite", action="store_true",
                     help="measure every workload (calibrated sweeps, fits, stability); JSON lines")
     ap.add_argument("--profile", action="store_true",
@@ -698,6 +745,8 @@ def main():
                     help="profiling: shrink the prefill workload to this many heads")
     ap.add_argument("--decode-batch", type=int, default=0,
                     help="profiling: shrink the decode workload to this many sequences")
+    ap.add_argument("--mla-batch", type=int, default=0,
+                    help="profiling: shrink the latent-attention suite workload to this many sequences")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -93,15 +93,63 @@ def decode(q, k, v, *, scale: float, lam: float = 0.0, num_kv_splits: int = 1, c
     return o
 
 
+MLA_LATENT, MLA_ROPE = 512, 64
+
+
+def mla_workspace(B, Hq, num_kv_splits, device, d_latent=MLA_LATENT):
+    import torch
+
+    n = capi.ss_attn_mla_decode_workspace_size(B, Hq, d_latent, num_kv_splits)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device), n
+
+
+def mla_decode(q, kv, *, scale: float, lam: float = 0.0, num_kv_splits: int = 1, counts=None,
+               out=None, workspace=None, skip_mask=None, vote_margin=None, stream=None,
+               d_latent: int = MLA_LATENT):
+    """Latent-attention (MLA) split-KV decode: q [B,Hq,dk] and one latent
+    cache kv [B,Lk,dk] (dk = d_latent + d_rope) bf16 CUDA; the values are
+    kv[..., :d_latent].  Returns o [B,Hq,d_latent]."""
+    import torch
+
+    B, Hq, dk = q.shape
+    Bk, Lk, dk2 = kv.shape
+    if Bk != B or dk2 != dk:
+        raise ValueError("mla_decode expects q [B,Hq,dk] and kv [B,Lk,dk]")
+    o = out if out is not None else torch.empty((B, Hq, d_latent), dtype=q.dtype, device=q.device)
+    if workspace is None:
+        workspace, nbytes = mla_workspace(B, Hq, num_kv_splits, q.device, d_latent)
+    else:
+        nbytes = workspace.numel() * workspace.element_size()
+    if skip_mask is None and vote_margin is None:
+        st = capi.ss_attn_mla_decode(q, kv, o, B, Hq, Lk, d_latent, dk - d_latent, scale, lam,
+                                     num_kv_splits, counts, workspace, nbytes, stream)
+    else:
+        st = capi.ss_attn_mla_decode_ex(q, kv, o, B, Hq, Lk, d_latent, dk - d_latent, scale, lam,
+                                        num_kv_splits, counts, workspace, nbytes, skip_mask,
+                                        vote_margin, False, stream)
+    _check(st, "ss_attn_mla_decode")
+    return o
+
+
 def calibrate(kind: str, q, k, v, *, scale: float, target_sparsity: float, causal: bool = False,
               num_kv_splits: int = 1, counts=None, stream=None):
-    """Fit a (lambda = a / Lk) for a target tile sparsity.  Returns (a, achieved)."""
+    """Fit a (lambda = a / Lk) for a target tile sparsity.  Returns (a, achieved).
+
+    kind: "prefill", "decode" or "mla_decode" (k is then the latent cache
+    [B,Lk,dk] and v is ignored)."""
     import torch
 
     if kind == "prefill":
         B, Hq, Hkv, Lq, Lk, d = _shape_prefill(q, k)
         n = units_prefill(B, Hq, Lq)
         k_ = capi.SS_PREFILL
+    elif kind == "mla_decode":
+        B, Hq, d = q.shape
+        Lk = k.shape[1]
+        Hkv, Lq = 1, 1
+        n = B * num_kv_splits
+        k_ = capi.SS_MLA_DECODE
+        v = k
     else:
         B, Hq, d = q.shape
         _, Hkv, Lk, _ = k.shape

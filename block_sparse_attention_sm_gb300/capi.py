@@ -15,12 +15,13 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libssattn.so")
 
 SS_OK, SS_ERR_INVALID_ARG, SS_ERR_UNSUPPORTED, SS_ERR_CUDA, SS_ERR_TIMEOUT, SS_ERR_WORKSPACE = range(6)
-SS_PREFILL, SS_DECODE = 0, 1
+SS_PREFILL, SS_DECODE, SS_MLA_DECODE = 0, 1, 2
 
 EXPORTS = (
     "ss_attn_prefill", "ss_attn_prefill_ex", "ss_attn_decode_workspace_size", "ss_attn_decode",
-    "ss_attn_decode_ex", "ss_attn_decode_noalloc", "ss_attn_decode_paged", "ss_calibrate",
-    "ss_fit_factor", "ss_lambda", "ss_status_string", "ss_stream_status",
+    "ss_attn_decode_ex", "ss_attn_decode_noalloc", "ss_attn_decode_paged",
+    "ss_attn_mla_decode_workspace_size", "ss_attn_mla_decode", "ss_attn_mla_decode_ex",
+    "ss_calibrate", "ss_fit_factor", "ss_lambda", "ss_status_string", "ss_stream_status",
 )
 
 
@@ -69,6 +70,11 @@ def load() -> ctypes.CDLL:
                                          ctypes.POINTER(ss_debug_opts), P]
     lib.ss_attn_decode_workspace_size.argtypes = [I, I, I, I]
     lib.ss_attn_decode_workspace_size.restype = U
+    mla = [P, P, P, I, I, I, I, I, F, F, I, P, P, U]
+    lib.ss_attn_mla_decode.argtypes = mla + [P]
+    lib.ss_attn_mla_decode_ex.argtypes = mla + [ctypes.POINTER(ss_debug_opts), P]
+    lib.ss_attn_mla_decode_workspace_size.argtypes = [I, I, I, I]
+    lib.ss_attn_mla_decode_workspace_size.restype = U
     lib.ss_calibrate.argtypes = [ctypes.POINTER(ss_problem), F, ctypes.POINTER(F), ctypes.POINTER(F)]
     lib.ss_fit_factor.argtypes = [ctypes.POINTER(F), ctypes.POINTER(F), I, ctypes.POINTER(F),
                                   ctypes.POINTER(F)]
@@ -78,8 +84,8 @@ def load() -> ctypes.CDLL:
     lib.ss_status_string.restype = ctypes.c_char_p
     lib.ss_stream_status.argtypes = [P]
     for name in ("ss_attn_prefill", "ss_attn_prefill_ex", "ss_attn_decode", "ss_attn_decode_ex",
-                 "ss_attn_decode_noalloc", "ss_attn_decode_paged", "ss_calibrate", "ss_fit_factor",
-                 "ss_stream_status"):
+                 "ss_attn_decode_noalloc", "ss_attn_decode_paged", "ss_attn_mla_decode",
+                 "ss_attn_mla_decode_ex", "ss_calibrate", "ss_fit_factor", "ss_stream_status"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -172,6 +178,29 @@ def ss_attn_decode_paged(q, k_pages, v_pages, page_table, seq_lens, o, B, Hq, Hk
 
 
 SS_DECODE_STATIC_SCRATCH_BYTES = 16 << 20
+
+
+def ss_attn_mla_decode_workspace_size(B, Hq, d_latent, num_kv_splits) -> int:
+    return int(load().ss_attn_mla_decode_workspace_size(B, Hq, d_latent, num_kv_splits))
+
+
+def ss_attn_mla_decode(q, kv, o, B, Hq, Lk, d_latent, d_rope, scale, lam, num_kv_splits,
+                       skip_counts=None, workspace=None, workspace_bytes=0, stream=None) -> int:
+    """Latent-attention decode: q [B,Hq,dk], one latent cache kv [B,Lk,dk]."""
+    return load().ss_attn_mla_decode(_ptr(q), _ptr(kv), _ptr(o), B, Hq, Lk, d_latent, d_rope,
+                                     float(scale), float(lam), int(num_kv_splits),
+                                     _ptr(skip_counts), _ptr(workspace), int(workspace_bytes),
+                                     _stream(stream))
+
+
+def ss_attn_mla_decode_ex(q, kv, o, B, Hq, Lk, d_latent, d_rope, scale, lam, num_kv_splits,
+                          skip_counts=None, workspace=None, workspace_bytes=0, skip_mask=None,
+                          vote_margin=None, count_only=False, stream=None) -> int:
+    dbg = _dbg(skip_mask, vote_margin, count_only)
+    return load().ss_attn_mla_decode_ex(_ptr(q), _ptr(kv), _ptr(o), B, Hq, Lk, d_latent, d_rope,
+                                        float(scale), float(lam), int(num_kv_splits),
+                                        _ptr(skip_counts), _ptr(workspace), int(workspace_bytes),
+                                        ctypes.byref(dbg), _stream(stream))
 
 
 def ss_calibrate(problem: ss_problem, target_sparsity: float):

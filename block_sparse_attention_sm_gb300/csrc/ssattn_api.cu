@@ -9,6 +9,7 @@
 #include <vector>
 
 #include "common.cuh"
+#include "mla.cuh"
 
 namespace ssattn {
 
@@ -203,11 +204,59 @@ ss_status decode_impl(const void* q, const void* k, const void* v, void* o, int 
   return e == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
+size_t mla_ws(int B, int Hq, int d_latent, int S) {
+  if (S <= 1 || B < 1 || Hq < 1 || d_latent < 1) return 0;
+  return static_cast<size_t>(B) * Hq * S * (d_latent + 2) * sizeof(float);
+}
+
+ss_status mla_impl(const void* q, const void* kv, void* o, int B, int Hq, int Lk, int d_latent,
+                   int d_rope, float scale, bool dense, float thr_raw, int S, uint32_t* counts,
+                   void* ws, size_t ws_bytes, const ss_debug_opts* dbg, void* stream) {
+  const bool count_only = dbg != nullptr && dbg->count_only != 0;
+  if (q == nullptr || kv == nullptr || (o == nullptr && !count_only)) return SS_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kv) || (o != nullptr && !aligned16(o))) return SS_ERR_INVALID_ARG;
+  if (B < 1 || Hq < 1 || Lk < 1 || S < 1 || !scale_ok(scale)) return SS_ERR_INVALID_ARG;
+  if (d_latent != kMlaLatent || d_rope != kMlaRope || Hq > kMlaMaxHeads) return SS_ERR_UNSUPPORTED;
+  const long nT = ceil_div(Lk, kTile);
+  if (static_cast<long>(B) * S > 0x7fffffffL) return SS_ERR_INVALID_ARG;
+  if (!count_only && S > 1) {
+    if (ws == nullptr || !aligned16(ws) || ws_bytes < mla_ws(B, Hq, d_latent, S))
+      return SS_ERR_WORKSPACE;
+  }
+  ss_status st = check_device();
+  if (st != SS_OK) return st;
+  // [B][Lk][576] viewed as B rows of Lk keys: 64 x 128 boxes, 128-byte swizzle.
+  CUtensorMap tkv;
+  if (!make_map(&tkv, kv, kMlaDk, Lk, B)) return SS_ERR_CUDA;
+
+  MlaParams p{};
+  p.B = B;
+  p.Hq = Hq;
+  p.Lk = Lk;
+  p.nT = static_cast<int>(nT);
+  p.S = S;
+  p.T = static_cast<int>(ceil_div(nT, S));
+  p.scale = scale;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.thr_raw = thr_raw;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.part = static_cast<float*>(ws);
+  p.counts = counts;
+  p.mask = dbg ? dbg->skip_mask : nullptr;
+  p.margin = dbg ? dbg->vote_margin : nullptr;
+  p.status = status_ptr();
+  const Mode mode = count_only ? Mode::kCount : (dense ? Mode::kDense : Mode::kSparse);
+  cudaError_t e = launch_mla_decode(tkv, p, mode, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+}
+
 // Evaluated (unit, tile) pairs of a problem (tiles a causal row block never
 // reaches are not evaluated).
 long evaluated_tiles(const ss_problem& p) {
   const long nT = ceil_div(p.Lk, kTile);
   if (p.kind == SS_DECODE) return static_cast<long>(p.B) * p.Hkv * nT;
+  if (p.kind == SS_MLA_DECODE) return static_cast<long>(p.B) * nT;
   const long nQB = ceil_div(p.Lq, kTile);
   long per_head = 0;
   for (long qb = 0; qb < nQB; ++qb) {
@@ -224,6 +273,7 @@ long evaluated_tiles(const ss_problem& p) {
 
 long counter_len(const ss_problem& p) {
   if (p.kind == SS_DECODE) return static_cast<long>(p.B) * p.Hkv * p.num_kv_splits;
+  if (p.kind == SS_MLA_DECODE) return static_cast<long>(p.B) * p.num_kv_splits;
   return static_cast<long>(p.B) * p.Hq * ceil_div(p.Lq, kTile);
 }
 
@@ -301,6 +351,33 @@ ss_status ss_attn_decode(const void* q, const void* k_cache, const void* v_cache
                          size_t workspace_bytes, void* stream) {
   return ss_attn_decode_ex(q, k_cache, v_cache, o, B, Hq, Hkv, Lk, d, scale, lambda,
                            num_kv_splits, skip_counts, workspace, workspace_bytes, nullptr, stream);
+}
+
+size_t ss_attn_mla_decode_workspace_size(int B, int Hq, int d_latent, int num_kv_splits) {
+  return mla_ws(B, Hq, d_latent, num_kv_splits);
+}
+
+ss_status ss_attn_mla_decode_ex(const void* q, const void* kv, void* o, int B, int Hq, int Lk,
+                                int d_latent, int d_rope, float scale, float lambda,
+                                int num_kv_splits, uint32_t* skip_counts, void* workspace,
+                                size_t workspace_bytes, const ss_debug_opts* dbg, void* stream) {
+  if (!lambda_ok(lambda)) return SS_ERR_INVALID_ARG;
+  const bool dense = lambda == 0.f;
+  const float thr = dense ? -INFINITY : threshold_raw(std::log(static_cast<double>(lambda)), scale);
+  // Debug outputs need the vote: with lambda = 0 it runs with a threshold
+  // no tile passes (every tile kept, margins reported).
+  const bool debug_out = dbg != nullptr && (dbg->skip_mask != nullptr || dbg->vote_margin != nullptr);
+  return mla_impl(q, kv, o, B, Hq, Lk, d_latent, d_rope, scale, dense && !debug_out, thr,
+                  num_kv_splits, skip_counts, workspace, workspace_bytes, dbg, stream);
+}
+
+ss_status ss_attn_mla_decode(const void* q, const void* kv, void* o, int B, int Hq, int Lk,
+                             int d_latent, int d_rope, float scale, float lambda,
+                             int num_kv_splits, uint32_t* skip_counts, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  return ss_attn_mla_decode_ex(q, kv, o, B, Hq, Lk, d_latent, d_rope, scale, lambda,
+                               num_kv_splits, skip_counts, workspace, workspace_bytes, nullptr,
+                               stream);
 }
 
 ss_status ss_attn_decode_paged(const void* q, const void* k_pages, const void* v_pages,
@@ -388,7 +465,9 @@ ss_status ss_calibrate(const ss_problem* p, float target_sparsity, float* a_out,
   if (p == nullptr || a_out == nullptr || p->skip_counts == nullptr || !aligned16(p->q) ||
       !(target_sparsity >= 0.f && target_sparsity <= 1.f) || p->Lk < 1)
     return SS_ERR_INVALID_ARG;
-  if (p->kind != SS_PREFILL && p->kind != SS_DECODE) return SS_ERR_INVALID_ARG;
+  if (p->kind != SS_PREFILL && p->kind != SS_DECODE && p->kind != SS_MLA_DECODE)
+    return SS_ERR_INVALID_ARG;
+  if (p->kind == SS_MLA_DECODE && (p->Hkv != 1 || p->d != kMlaDk)) return SS_ERR_UNSUPPORTED;
   const long N = evaluated_tiles(*p);
   const long ncnt = counter_len(*p);
   if (N <= 0 || ncnt <= 0) return SS_ERR_INVALID_ARG;
@@ -406,6 +485,9 @@ ss_status ss_calibrate(const ss_problem* p, float target_sparsity, float* a_out,
     if (p->kind == SS_PREFILL)
       st = prefill_impl(p->q, p->k, p->v, nullptr, p->B, p->Hq, p->Hkv, p->Lq, p->Lk, p->d,
                         p->scale, p->causal, false, thr, p->skip_counts, &dbg, p->stream);
+    else if (p->kind == SS_MLA_DECODE)
+      st = mla_impl(p->q, p->k, nullptr, p->B, p->Hq, p->Lk, kMlaLatent, kMlaRope, p->scale,
+                    false, thr, p->num_kv_splits, p->skip_counts, nullptr, 0, &dbg, p->stream);
     else
       st = decode_impl(p->q, p->k, p->v, nullptr, p->B, p->Hq, p->Hkv, p->Lk, p->d, p->scale,
                        false, thr, p->num_kv_splits, p->skip_counts, nullptr, 0, &dbg, p->stream);

@@ -167,11 +167,11 @@ WORKLOADS = {
     "llama_chunked_prefill_2k_on_32k": dict(kind="prefill", B=4, Hq=32, Hkv=8, Lq=2048,
                                             Lk=32768, d=128, causal=True, scale=128 ** -0.5,
                                             hot_frac=0.10, per_head_u=True),
-    # latent-attention decode (absorbed form): 16 query heads sharing one
-    # latent head of 512 + 64 rotary dims (DeepSeek-V2-Lite's heads, or
-    # DeepSeek-V3's 128 over 8 GPUs); softmax scale 1/sqrt(128 + 64)
-    "mla_decode_32k": dict(kind="mla_decode", B=64, Hq=16, Lk=32768, d_latent=512, d_rope=64,
-                           scale=192 ** -0.5, hot_frac=0.10, num_splits=16),
+    # latent-attention decode (absorbed form): 128 sequences, 16 query heads
+    # sharing one latent head of 512 + 64 rotary dims (DeepSeek-V2-Lite's
+    # heads, or DeepSeek-V3's 128 over 8 GPUs); softmax scale 1/sqrt(128 + 64)
+    "mla_decode_32k": dict(kind="mla_decode", B=128, Hq=16, Lk=32768, d_latent=512, d_rope=64,
+                           scale=192 ** -0.5, hot_frac=0.10, num_splits=4),
     "long_prefill_128k": dict(kind="prefill", B=1, Hq=32, Hkv=8, Lq=131072, Lk=131072, d=128,
                               causal=True, scale=128 ** -0.5, hot_frac=0.05, per_head_u=True),
     "long_decode_128k": dict(kind="decode", B=8, Hq=32, Hkv=8, Lk=131072, d=128,

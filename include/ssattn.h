@@ -60,8 +60,9 @@ extern "C" {
 typedef enum {
   SS_OK = 0,
   SS_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad shape, lambda or scale */
-  SS_ERR_UNSUPPORTED = 2,  /* d not in {64,128}, decode with Hq/Hkv > 16, or the current
-                              device is not sm_103 */
+  SS_ERR_UNSUPPORTED = 2,  /* d not in {64,128}, decode with Hq/Hkv > 16, latent decode
+                              with other widths or Hq > 16, or the current device is not
+                              sm_103 */
   SS_ERR_CUDA = 3,         /* a CUDA runtime call failed (launch, copy, sync) */
   SS_ERR_TIMEOUT = 4,      /* a kernel's bounded wait expired (logic error; reported, not hung) */
   SS_ERR_WORKSPACE = 5     /* decode workspace missing or too small */
@@ -214,8 +215,49 @@ ss_status ss_attn_decode_noalloc(const void* q, const void* k_cache, const void*
                                  float lambda, int num_kv_splits, uint32_t* skip_counts,
                                  void* stream);
 
+/*
+ * Latent-attention (MLA) decode: the skip test on multi-head latent
+ * attention, which the "Skip-Softmax" design doc lists among the supported
+ * attention kinds without giving its shapes.  Read as the absorbed decode
+ * form: each sequence caches one latent row per token, d_latent latent
+ * entries followed by d_rope rotary entries; the keys are the whole rows
+ * (width dk = d_latent + d_rope), the values their first d_latent entries,
+ * and every query head attends to that one latent head.  All Hq heads of a
+ * sequence are therefore the voting group of a tile: a tile is skipped only
+ * if exp(tile_max - running_max) < lambda holds for every head (BLASST
+ * summary, §Methodologie; "Skip-Softmax" §What this bounds).  The split of
+ * the nT = ceil(Lk/128) tiles into num_kv_splits contiguous ranges and the
+ * log-sum-exp merge are those of ss_attn_decode.  The values are read from
+ * the key rows already on chip, so a skipped tile saves the exponentials and
+ * the P.V products, not memory traffic.
+ *   q:  [B][Hq][dk] bf16 (the absorbed queries), 16-byte aligned.
+ *   kv: [B][Lk][dk] bf16 latent cache, contiguous, 16-byte aligned.
+ *   o:  [B][Hq][d_latent] bf16.
+ *   Only d_latent = 512, d_rope = 64 and 1 <= Hq <= 16 are supported.
+ *   skip_counts: nullable device buffer [B*num_kv_splits]; overwritten.
+ *   workspace: device buffer of at least
+ *     ss_attn_mla_decode_workspace_size(B, Hq, d_latent, num_kv_splits)
+ *     bytes, 16-byte aligned (may be NULL when that size is 0).
+ *   dbg (the _ex form): skip_mask / vote_margin are [B][nT]; count_only as
+ *     elsewhere.
+ * Returns SS_OK, SS_ERR_INVALID_ARG (null or misaligned pointer, B, Hq, Lk or
+ * num_kv_splits < 1, lambda outside [0, 1], scale <= 0), SS_ERR_UNSUPPORTED,
+ * SS_ERR_WORKSPACE or SS_ERR_CUDA.  Asynchronous on `stream`.
+ */
+size_t ss_attn_mla_decode_workspace_size(int B, int Hq, int d_latent, int num_kv_splits);
+
+ss_status ss_attn_mla_decode(const void* q, const void* kv, void* o, int B, int Hq, int Lk,
+                             int d_latent, int d_rope, float scale, float lambda,
+                             int num_kv_splits, uint32_t* skip_counts, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+ss_status ss_attn_mla_decode_ex(const void* q, const void* kv, void* o, int B, int Hq, int Lk,
+                                int d_latent, int d_rope, float scale, float lambda,
+                                int num_kv_splits, uint32_t* skip_counts, void* workspace,
+                                size_t workspace_bytes, const ss_debug_opts* dbg, void* stream);
+
 /* A calibration problem: the inputs the threshold is fitted on. */
-typedef enum { SS_PREFILL = 0, SS_DECODE = 1 } ss_kind;
+typedef enum { SS_PREFILL = 0, SS_DECODE = 1, SS_MLA_DECODE = 2 } ss_kind;
 typedef struct {
   ss_kind kind;
   const void* q;
@@ -228,8 +270,11 @@ typedef struct {
   float scale;
   int causal;      /* prefill only */
   int num_kv_splits; /* decode only */
+  /* SS_MLA_DECODE: k is the latent cache [B][Lk][d], v is ignored, Hkv is 1
+     and d is the key width d_latent + d_rope (576, of which 512 latent). */
   /* Device buffer for the per-unit counters, sized as the matching call's
-     skip_counts (prefill: B*Hq*ceil(Lq/128); decode: B*Hkv*num_kv_splits). */
+     skip_counts (prefill: B*Hq*ceil(Lq/128); decode: B*Hkv*num_kv_splits;
+     latent decode: B*num_kv_splits). */
   uint32_t* skip_counts;
   void* stream;
 } ss_problem;

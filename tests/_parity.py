@@ -196,6 +196,58 @@ def check_decode(q, k, v, *, scale, lam, num_splits, units=None):
     return n_dis
 
 
+def check_mla(q, kv, *, scale, lam, num_splits, units=None, d_latent=512):
+    """Parity of one latent-attention decode launch; `units` = sequences."""
+    B, Hq, dk = q.shape
+    Lk = kv.shape[1]
+    nT = -(-Lk // TILE)
+    S = num_splits
+    dev = q.device
+    ws_n = capi.ss_attn_mla_decode_workspace_size(B, Hq, d_latent, S)
+    ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=dev)
+    o = torch.full((B, Hq, d_latent), float("nan"), dtype=q.dtype, device=dev)
+    counts = torch.full((B * S,), -1, dtype=torch.int32, device=dev)
+    st = capi.ss_attn_mla_decode(q, kv, o, B, Hq, Lk, d_latent, dk - d_latent, scale, lam, S,
+                                 counts, ws, ws_n)
+    assert st == capi.SS_OK, capi.ss_status_string(st)
+    o2 = torch.full_like(o, float("nan"))
+    counts2 = torch.full_like(counts, -1)
+    mask = torch.full((B, nT), 7, dtype=torch.uint8, device=dev)
+    margin = torch.full((B, nT), 12345.0, dtype=torch.float32, device=dev)
+    st = capi.ss_attn_mla_decode_ex(q, kv, o2, B, Hq, Lk, d_latent, dk - d_latent, scale, lam, S,
+                                    counts2, ws, ws_n, mask, margin)
+    assert st == capi.SS_OK, capi.ss_status_string(st)
+    assert capi.ss_stream_status() == capi.SS_OK
+    torch.cuda.synchronize()
+    if lam > 0:
+        assert torch.equal(o, o2) and torch.equal(counts, counts2)
+    else:  # the plain call runs the dense kernel, the debug call the voting one
+        assert torch.equal(counts, counts2)
+        check_output(o.float().cpu().numpy(), o2.double().cpu().numpy(), "dense vs voting kernel")
+    units = sorted(range(B) if units is None else units)
+    ch = counts.cpu().numpy().reshape(B, S)
+    mh, gh = mask.cpu().numpy(), margin.cpu().numpy()
+    og = o.float().cpu().numpy()
+    T = -(-nT // S)
+    n_dis = 0
+    for b in units:
+        qs, kvs = q[b:b + 1], kv[b:b + 1]
+        ref = oracle.mla_decode(qs, kvs, d_latent=d_latent, scale=scale, lam=lam, num_splits=S)
+        nd, row_dis = compare_decisions(mh[b:b + 1], gh[b:b + 1], ref.mask, ref.margin, lam)
+        n_dis += nd
+        for sp in range(S):
+            tiles = list(range(sp * T, min(nT, sp * T + T)))
+            assert ch[b, sp] == (int((mh[b, tiles] == 1).sum()) if tiles else 0)
+            if not row_dis[0]:
+                assert ch[b, sp] == ref.counts[0, sp]
+        over = oracle.mla_decode(qs, kvs, d_latent=d_latent, scale=scale, lam=lam, num_splits=S,
+                                 mask_override=(mh[b:b + 1] == 1).astype(np.uint8))
+        check_output(og[b], over.o[0], f"mla sequence {b} under GPU mask")
+        if not row_dis[0]:
+            check_output(og[b], ref.o[0], f"mla sequence {b}")
+    return n_dis
+
+
 def hot_prefill(B, Hq, Hkv, Lq, Lk, d, frac=0.2, seed=0, per_head_u=True):
     inp = synth.prefill_inputs(B=B, Hq=Hq, Hkv=Hkv, Lq=Lq, Lk=Lk, d=d, hot_frac=frac, seed=seed,
                                per_head_u=per_head_u, device="cuda")

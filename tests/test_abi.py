@@ -127,6 +127,40 @@ def test_paged_decode_rejects_before_launch(capi, kw, expect):
     assert st == getattr(capi, expect)
 
 
+@pytest.mark.parametrize("kw,expect", [
+    (dict(q=None), "SS_ERR_INVALID_ARG"),
+    (dict(kv=FAKE + 8), "SS_ERR_INVALID_ARG"),     # misaligned cache
+    (dict(B=0), "SS_ERR_INVALID_ARG"),
+    (dict(Lk=0), "SS_ERR_INVALID_ARG"),
+    (dict(S=0), "SS_ERR_INVALID_ARG"),
+    (dict(lam=1.5), "SS_ERR_INVALID_ARG"),
+    (dict(scale=0.0), "SS_ERR_INVALID_ARG"),
+    (dict(Hq=17), "SS_ERR_UNSUPPORTED"),            # voting group wider than the MMA's N
+    (dict(d_latent=256), "SS_ERR_UNSUPPORTED"),
+    (dict(d_rope=32), "SS_ERR_UNSUPPORTED"),
+    (dict(S=4, ws_bytes=16), "SS_ERR_WORKSPACE"),
+])
+def test_mla_decode_rejects_before_launch(capi, kw, expect):
+    args = dict(q=FAKE, kv=FAKE, B=2, Hq=16, Lk=1000, d_latent=512, d_rope=64, scale=0.07,
+                lam=0.01, S=1, ws=FAKE, ws_bytes=1 << 30)
+    args.update(kw)
+    st = capi.ss_attn_mla_decode(args["q"], args["kv"], FAKE, args["B"], args["Hq"], args["Lk"],
+                                 args["d_latent"], args["d_rope"], args["scale"], args["lam"],
+                                 args["S"], None, args["ws"], args["ws_bytes"], stream=0)
+    assert st == getattr(capi, expect)
+
+
+def test_mla_calibration_problem_checks(capi):
+    """A latent-attention calibration problem must have one KV head and the
+    576-entry key width; checked before anything runs."""
+    cnt = FAKE
+    for Hkv, d in ((2, 576), (1, 128)):
+        prob = capi.ss_problem(capi.SS_MLA_DECODE, FAKE, FAKE, None, 2, 16, Hkv, 1, 1000, d, 0.07,
+                               0, 1, cnt, 0)
+        st, _, _ = capi.ss_calibrate(prob, 0.5)
+        assert st == capi.SS_ERR_UNSUPPORTED
+
+
 def test_struct_layouts_match_the_header(capi, tmp_path):
     """ctypes mirrors of the C structs have the C compiler's sizes and offsets."""
     src = tmp_path / "sz.c"
@@ -149,6 +183,8 @@ def test_struct_layouts_match_the_header(capi, tmp_path):
 def test_workspace_size(capi):
     assert capi.ss_attn_decode_workspace_size(64, 32, 128, 1) == 0
     assert capi.ss_attn_decode_workspace_size(64, 32, 128, 8) == 64 * 32 * 8 * 130 * 4
+    assert capi.ss_attn_mla_decode_workspace_size(64, 16, 512, 1) == 0
+    assert capi.ss_attn_mla_decode_workspace_size(64, 16, 512, 16) == 64 * 16 * 16 * 514 * 4
 
 
 def test_product_does_not_import_the_oracle():
