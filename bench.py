@@ -546,6 +546,33 @@ def run_suite(args):
         del q, kv, o, inp
         torch.cuda.empty_cache()
 
+    def sdpa_points(name):
+        """Sanity check of the dense denominator: PyTorch's
+        scaled_dot_product_attention (its default backend on this GPU) against
+        this library's lambda = 0 path, same bf16 inputs and shapes."""
+        import torch.nn.functional as F
+
+        inp, cfg = synth.make(name, seed=0, device=dev)
+        q, k, v = inp.q, inp.k, inp.v
+        B, Hq, Lq, d = q.shape
+        Hkv, Lk = k.shape[1], k.shape[2]
+        causal = cfg["causal"]
+        flops = 4.0 * B * Hq * Lq * Lk * d * (0.5 if causal else 1.0)
+        o = torch.empty_like(q)
+        ms_own = _time_ms(lambda: ss.prefill(q, k, v, scale=cfg["scale"], causal=causal, lam=0.0, out=o))
+        kw = {"enable_gqa": True} if Hkv != Hq else {}
+        ms_sdpa = _time_ms(lambda: F.scaled_dot_product_attention(q, k, v, is_causal=causal,
+                                                                   scale=cfg["scale"], **kw))
+        ref = F.scaled_dot_product_attention(q, k, v, is_causal=causal, scale=cfg["scale"], **kw)
+        diff = (ref.float() - o.float()).abs()
+        emit({"suite": name, "kind": "sdpa_sanity", "own_dense_ms": round(ms_own, 4),
+              "own_dense_tflops": round(flops / ms_own / 1e9, 1), "sdpa_ms": round(ms_sdpa, 4),
+              "sdpa_tflops": round(flops / ms_sdpa / 1e9, 1),
+              "own_vs_sdpa": round(ms_sdpa / ms_own, 3),
+              "max_abs_diff": round(float(diff.max()), 5), "mean_abs_diff": float(diff.mean())})
+        del q, k, v, o, ref, inp
+        torch.cuda.empty_cache()
+
     def paged_points():
         """Paged, ragged decode: 64 sequences of 8K..32K keys in shuffled pages
         of 128 keys, lambda_b = a / L_b per sequence with the a calibrated for
@@ -604,7 +631,7 @@ def run_suite(args):
         torch.cuda.empty_cache()
 
     parts = set(filter(None, args.suite_only.split(","))) or {"prefill", "chunked", "decode", "paged",
-                                                                  "mla", "stability"}
+                                                                  "mla", "sdpa", "stability"}
     if "prefill" in parts:
         prefill_points("tiny_prefill", [0.0, 0.5, 0.75])
         prefill_points("dit_prefill_32k", [0.0, 0.5, 0.7])
@@ -621,6 +648,9 @@ def run_suite(args):
         paged_points()
     if "mla" in parts:
         mla_points("mla_decode_32k", [0.0, 0.5, 0.7, 0.9])
+    if "sdpa" in parts:
+        sdpa_points("dit_prefill_32k")
+        sdpa_points("llama_prefill_16k")
     if "stability" in parts:
         stability()
 
@@ -736,7 +766,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--suite-only", default="",
-                    help="with --suite: run only the named parts (comma-separated: prefill, chunked, decode, paged, mla, stability)")
+                    help="with --suite: run only the named parts (comma-separated: prefill, chunked, decode, paged, mla, sdpa, stability)")
     ap.add_argument("--suite", action="store_true",
                     help="measure every workload (calibrated sweeps, fits, stability); JSON lines")
     ap.add_argument("--profile", action="store_true",
