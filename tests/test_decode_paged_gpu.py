@@ -160,3 +160,21 @@ def test_paged_matches_contiguous_layout():
     assert torch.equal(c1, c2)
     diff = (o1.float() - o2.float()).abs().max().item()
     assert diff <= 1e-6, diff
+
+
+@pytest.mark.slow
+def test_paged_full_size_sampled():
+    """The bench's paged workload (64 sequences of 8K..32K keys in shuffled
+    pages, 8 splits) at the a calibrated for 70% on the contiguous cache, in
+    one launch; the oracle checks every sequence."""
+    import block_sparse_attention_sm_gb300 as ss
+    from block_sparse_attention_sm_gb300 import synth
+
+    B, Hq, Hkv, d, S, Lmax = 64, 32, 8, 128, 8, 32768
+    rng = np.random.default_rng(7)
+    lens = [int(x) for x in rng.integers(8192, Lmax + 1, size=B)]
+    inp = synth.decode_inputs(B=B, Hq=Hq, Hkv=Hkv, Lk=Lmax, d=d, hot_frac=0.10, seed=0,
+                              device="cuda")
+    a, _ = ss.calibrate("decode", inp.q, inp.k, inp.v, scale=d ** -0.5, target_sparsity=0.7,
+                        num_kv_splits=S)
+    check_paged(inp.q, inp.k, inp.v, lens, scale=d ** -0.5, a=a, num_splits=S, seed=11)

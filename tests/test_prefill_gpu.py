@@ -112,9 +112,10 @@ def test_random_scores_many_decisions():
 
 
 def _sampled_units(B, Hq, nqb, heads, rng):
+    """Query blocks 0, last and six random ones of each sampled head (batch 0)."""
     units = []
     for h in heads:
-        for qb in sorted({0, nqb - 1, *rng.choice(nqb, size=3, replace=False).tolist()}):
+        for qb in sorted({0, nqb - 1, *rng.choice(nqb, size=6, replace=False).tolist()}):
             units.append((0, int(h), int(qb)))
     return units
 
@@ -131,7 +132,7 @@ def test_full_size_sampled(workload, a):
     inp, cfg = synth.make(workload, seed=0, device="cuda")
     rng = np.random.default_rng(11)
     nqb = -(-cfg["Lq"] // 128)
-    heads = sorted(rng.choice(cfg["Hq"], size=2, replace=False).tolist())
+    heads = sorted(rng.choice(cfg["Hq"], size=4, replace=False).tolist())
     units = _sampled_units(1, cfg["Hq"], nqb, heads, rng)
     check_prefill(inp.q, inp.k, inp.v, scale=cfg["scale"], causal=cfg["causal"],
                   lam=a / cfg["Lk"], units=units)
