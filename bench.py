@@ -118,6 +118,25 @@ def _dist():
     return ws, rank, local
 
 
+def max_over_ranks(values, ws, device="cpu"):
+    """The slowest rank sets the job's time: element-wise maximum over ranks
+    (a process group must be initialised when ws > 1)."""
+    if ws <= 1:
+        return [float(x) for x in values]
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(x) for x in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_rate(work_per_rank, ws, ms):
+    """Whole-job throughput of N independent replicas (weak scaling): every
+    rank processes the same work, and the job takes the slowest rank's time."""
+    return work_per_rank * ws / ms
+
+
 def prefill_flops(B, Hq, nqb, nT_eval, kept, d):
     """Executed FLOPs: Q K^T on every evaluated tile, P.V on kept tiles."""
     return 2 * TILE * TILE * d * (nT_eval + kept)
@@ -242,12 +261,9 @@ def run_native(args):
     bytes_d_part = 2 * dB * dHq * S * (dd + 2) * 4
 
     # max over ranks
-    if ws > 1:
-        t = torch.tensor([ms_p, ms_d, ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_p, ms_d, ms_step = t.tolist()
-    tflops = flops_p * ws / ms_p / 1e9
-    gbs = bytes_d * ws / ms_d / 1e6
+    ms_p, ms_d, ms_step = max_over_ranks([ms_p, ms_d, ms_step], ws, dev)
+    tflops = job_rate(flops_p, ws, ms_p) / 1e9
+    gbs = job_rate(bytes_d, ws, ms_d) / 1e6
 
     # ---------------------------------------------------------------- end to end (host buffers)
     e2e_steps = max(3, min(args.steps, 10))
@@ -274,10 +290,7 @@ def run_native(args):
     e1.record(stream)
     torch.cuda.synchronize()
     ms_e2e = e0.elapsed_time(e1) / e2e_steps
-    if ws > 1:
-        t = torch.tensor([ms_e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_e2e = t.item()
+    (ms_e2e,) = max_over_ranks([ms_e2e], ws, dev)
 
     line = None
     if rank == 0:
@@ -336,7 +349,7 @@ def run_native(args):
                 "peak_kind": f"HBM copy ({peaks['src']})",
             },
             "clocks": clk,
-            "e2e": {"value": round(flops_p * ws / ms_e2e / 1e9, 2), "unit": "TFLOP/s",
+            "e2e": {"value": round(job_rate(flops_p, ws, ms_e2e) / 1e9, 2), "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": round(ms_e2e, 4),
                     "what": "prefill through the C ABI with pinned host buffers: H2D q,k,v + "

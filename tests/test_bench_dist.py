@@ -1,0 +1,77 @@
+"""Multi-process host logic of bench.py on CPU (gloo, world size 2).
+
+One process per GPU runs an independent replica of the workload (the units
+shard with no exchange), the job time is the slowest rank's, and the whole-job
+rate is the ranks' total work over that time.  These tests run the same
+host code on CPU processes instead of GPUs.
+"""
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, ws, port, out):
+    import torch.distributed as dist
+
+    sys.path.insert(0, ROOT)
+    import bench
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(ws), LOCAL_RANK=str(rank))
+    assert bench._dist() == (ws, rank, rank)
+    dist.init_process_group("gloo", rank=rank, world_size=ws)
+    # rank r was slower on the first value, faster on the second
+    got = bench.max_over_ranks([1.0 + rank, 5.0 - rank, 2.5], ws)
+    out[rank] = torch.tensor(got + [bench.job_rate(100.0, ws, got[0])], dtype=torch.float64)
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_and_job_rate_gloo_world_size_2():
+    ws = 2
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    mgr = ctx.Manager()
+    out = mgr.dict()
+    procs = [ctx.Process(target=_worker, args=(r, ws, port, out)) for r in range(ws)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    for r in range(ws):
+        t = out[r].tolist()
+        assert t[:3] == [2.0, 5.0, 2.5]       # element-wise maximum over the ranks
+        assert t[3] == pytest.approx(100.0 * ws / 2.0)
+
+
+def test_single_process_needs_no_group():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    assert bench.max_over_ranks([3, 4], 1) == [3.0, 4.0]
+    assert bench.job_rate(10.0, 1, 2.0) == 5.0
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    """Under torchrun the oracle baseline runs on rank 0 only; other ranks
+    print nothing and exit 0."""
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "3", "--warmup", "3"], env=env, capture_output=True, text=True,
+                       timeout=300, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.strip() == ""
