@@ -44,7 +44,7 @@ template <int D, int GP>
 struct DecCfg {
   static constexpr int NQ = (GP <= 16) ? 16 : 32;  // MMA N (rows padded with zeros)
   static constexpr int NK = (D == 128) ? 4 : 8;    // K ring stages
-  static constexpr int NV = (D == 128) ? 2 : 4;    // V / P / O slots
+  static constexpr int NV = (D == 128 || GP > 16) ? 2 : 4;  // V / P / O slots
   static constexpr int NS = 4;                      // score buffers in TMEM
   static constexpr int kChunks = D / 64;            // 128-byte swizzle chunks per row
   static constexpr int kTileBytes = kTile * D * 2;
@@ -117,6 +117,12 @@ __device__ __forceinline__ void tmem_ld_cols<16>(uint32_t taddr, float (&r)[16])
         "=f"(r[7]), "=f"(r[8]), "=f"(r[9]), "=f"(r[10]), "=f"(r[11]), "=f"(r[12]), "=f"(r[13]),
         "=f"(r[14]), "=f"(r[15])
       : "r"(taddr));
+}
+
+template <>
+__device__ __forceinline__ void tmem_ld_cols<32>(uint32_t taddr, float (&r)[32]) {
+  tmem_ld_cols<16>(taddr, *reinterpret_cast<float(*)[16]>(&r[0]));
+  tmem_ld_cols<16>(taddr + 16, *reinterpret_cast<float(*)[16]>(&r[16]));
 }
 
 // Maximum over the warp (every lane gets it).
@@ -616,7 +622,8 @@ cudaError_t launch_dec_g(const CUtensorMap& tk, const CUtensorMap& tv, const Dec
   if (p.G <= 2) return launch_dec_mode<D, 2>(tk, tv, p, mode, st);
   if (p.G <= 4) return launch_dec_mode<D, 4>(tk, tv, p, mode, st);
   if (p.G <= 8) return launch_dec_mode<D, 8>(tk, tv, p, mode, st);
-  return launch_dec_mode<D, 16>(tk, tv, p, mode, st);
+  if (p.G <= 16) return launch_dec_mode<D, 16>(tk, tv, p, mode, st);
+  return launch_dec_mode<D, 32>(tk, tv, p, mode, st);
 }
 
 }  // namespace

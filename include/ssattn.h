@@ -60,7 +60,7 @@ extern "C" {
 typedef enum {
   SS_OK = 0,
   SS_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad shape, lambda or scale */
-  SS_ERR_UNSUPPORTED = 2,  /* d not in {64,128}, decode with Hq/Hkv > 16, latent decode
+  SS_ERR_UNSUPPORTED = 2,  /* d not in {64,128}, decode with Hq/Hkv > 32, latent decode
                               with other widths or Hq > 16, or the current device is not
                               sm_103 */
   SS_ERR_CUDA = 3,         /* a CUDA runtime call failed (launch, copy, sync) */

@@ -91,7 +91,7 @@ def test_prefill_rejects_before_launch(capi, kw, expect):
 @pytest.mark.parametrize("kw,expect", [
     (dict(S=0), "SS_ERR_INVALID_ARG"),
     (dict(Lk=0), "SS_ERR_INVALID_ARG"),
-    (dict(Hq=64, Hkv=2), "SS_ERR_UNSUPPORTED"),       # vote group > 16
+    (dict(Hq=66, Hkv=2), "SS_ERR_UNSUPPORTED"),       # vote group > 32
     (dict(S=4, ws=None), "SS_ERR_WORKSPACE"),
     (dict(S=4, ws_bytes=16), "SS_ERR_WORKSPACE"),
 ])
@@ -113,7 +113,7 @@ def test_decode_rejects_before_launch(capi, kw, expect):
     (dict(a=float("inf")), "SS_ERR_INVALID_ARG"),
     (dict(k=FAKE + 4), "SS_ERR_INVALID_ARG"),
     (dict(d=96), "SS_ERR_UNSUPPORTED"),
-    (dict(Hq=64, Hkv=2), "SS_ERR_UNSUPPORTED"),
+    (dict(Hq=66, Hkv=2), "SS_ERR_UNSUPPORTED"),
     (dict(S=4, ws=None), "SS_ERR_WORKSPACE"),
 ])
 def test_paged_decode_rejects_before_launch(capi, kw, expect):

@@ -29,8 +29,11 @@ SHAPES = [
     (1, 4, 1, 100, 128, 1),     # one partial tile
     (1, 4, 1, 300, 128, 8),     # more splits than tiles: empty splits
     (2, 8, 1, 900, 64, 3),      # d = 64 with an 8-row vote group
-    (1, 16, 1, 1000, 128, 2),   # G = 16 (the largest vote group)
+    (1, 16, 1, 1000, 128, 2),   # G = 16 (largest group of the 16-row MMA)
     (2, 24, 2, 700, 64, 1),     # G = 12 (padded to 16 rows)
+    (2, 32, 1, 3000, 128, 3),   # G = 32: MQA with 32 query heads (the largest vote group)
+    (2, 48, 2, 1300, 64, 2),    # G = 24 (padded to 32 rows), d = 64
+    (1, 17, 1, 640, 128, 1),    # G = 17: the smallest group of the 32-row MMA
 ]
 
 

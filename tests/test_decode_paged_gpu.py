@@ -116,6 +116,7 @@ CASES = [
     (3, 8, 2, 64, [700, 1, 5000], 1),
     (2, 16, 1, 128, [2500, 4096], 4),          # G = 16
     (4, 32, 8, 128, [333, 8191, 8192, 1], 8),  # Llama-shaped heads, ragged lengths
+    (3, 32, 1, 128, [4000, 129, 2048], 2),     # G = 32 (MQA)
 ]
 
 
