@@ -653,6 +653,7 @@ def run_suite(args):
         prefill_points("llama_chunked_prefill_2k_on_32k", [0.0, 0.5, 0.7, 0.9])
     if "decode" in parts:
         decode_points("llama_decode_32k", [0.0, 0.5, 0.7])
+        decode_points("mqa_decode_32k", [0.0, 0.5, 0.7])
     if "prefill" in parts:
         prefill_points("long_prefill_128k", [0.0, 0.5, 0.7, 0.9])
     if "decode" in parts:
