@@ -586,6 +586,60 @@ def run_suite(args):
         del q, k, v, o, ref, inp
         torch.cuda.empty_cache()
 
+    def mla_paged_points():
+        """Paged, ragged latent-attention decode: 128 sequences of 8K..32K
+        rows in shuffled pages of 128, lambda_b = a / L_b with the a
+        calibrated for 70% on the contiguous 32K cache of the same data."""
+        from block_sparse_attention_sm_gb300 import capi
+
+        B, Hq, S, Lmax = 128, 16, 4, 32768
+        rng = np.random.default_rng(9)
+        lens = [int(x) for x in rng.integers(8192, Lmax + 1, size=B)]
+        inp = synth.mla_decode_inputs(B=B, Hq=Hq, Lk=Lmax, hot_frac=0.10, seed=0, device=dev)
+        q, kv = inp.q, inp.kv
+        scale = 192 ** -0.5
+        a, _ = ss.calibrate("mla_decode", q, kv, None, scale=scale, target_sparsity=0.7,
+                            num_kv_splits=S)
+        npg = [-(-L // TILE) for L in lens]
+        num_pages, max_pages = sum(npg), max(npg)
+        perm = torch.from_numpy(rng.permutation(num_pages)).to(dev)
+        pages = torch.empty(num_pages, TILE, kv.shape[2], dtype=kv.dtype, device=dev)
+        table = torch.zeros(B, max_pages, dtype=torch.int32, device=dev)
+        off = 0
+        for b, n in enumerate(npg):
+            pg = perm[off:off + n]
+            off += n
+            pages[pg] = kv[b, :n * TILE].reshape(n, TILE, kv.shape[2])
+            table[b, :n] = pg.to(torch.int32)
+        del inp, kv
+        torch.cuda.empty_cache()
+        lens_t = torch.tensor(lens, dtype=torch.int32, device=dev)
+        cnt = torch.zeros(B * S, dtype=torch.int32, device=dev)
+        o = torch.empty(B, Hq, 512, dtype=q.dtype, device=dev)
+        wsn = capi.ss_attn_mla_decode_workspace_size(B, Hq, 512, S)
+        ws = torch.empty(wsn, dtype=torch.uint8, device=dev)
+        n_eval = num_pages
+        byts = sum(lens) * 576 * 2 + B * Hq * (576 + 512) * 2
+        dense_ms = None
+        for tag, aa in (("dense", 0.0), ("a_for_70pct_at_32k", a)):
+            def run():
+                st = capi.ss_attn_mla_decode_paged(q, pages, table, lens_t, o, B, Hq, num_pages,
+                                                   max_pages, 512, 64, scale, aa, S, cnt, ws, wsn)
+                if st != capi.SS_OK:
+                    raise SystemExit(capi.ss_status_string(st))
+            ms = _time_ms(run)
+            sk = int(cnt.sum())
+            if aa == 0.0:
+                dense_ms = ms
+            emit({"suite": "mla_paged_decode_ragged", "kind": "mla_decode", "point": tag, "a": aa,
+                  "lens": [min(lens), max(lens), sum(lens) // B], "pages": num_pages,
+                  "sparsity": round(sk / n_eval, 4), "ms": round(ms, 4),
+                  "gbs": round(byts / ms / 1e6, 1), "frac_of_peak": round(byts / ms / 1e6 / peaks["hbm"], 4),
+                  "tokens_per_s": round(B / ms * 1e3, 1),
+                  "speedup_vs_dense": round(dense_ms / ms, 3) if dense_ms else None})
+        del q, pages, o
+        torch.cuda.empty_cache()
+
     def paged_points():
         """Paged, ragged decode: 64 sequences of 8K..32K keys in shuffled pages
         of 128 keys, lambda_b = a / L_b per sequence with the a calibrated for
@@ -662,6 +716,7 @@ def run_suite(args):
         paged_points()
     if "mla" in parts:
         mla_points("mla_decode_32k", [0.0, 0.5, 0.7, 0.9])
+        mla_paged_points()
     if "sdpa" in parts:
         sdpa_points("dit_prefill_32k")
         sdpa_points("llama_prefill_16k")

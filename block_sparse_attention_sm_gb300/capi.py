@@ -21,6 +21,7 @@ EXPORTS = (
     "ss_attn_prefill", "ss_attn_prefill_ex", "ss_attn_decode_workspace_size", "ss_attn_decode",
     "ss_attn_decode_ex", "ss_attn_decode_noalloc", "ss_attn_decode_paged",
     "ss_attn_mla_decode_workspace_size", "ss_attn_mla_decode", "ss_attn_mla_decode_ex",
+    "ss_attn_mla_decode_paged",
     "ss_calibrate", "ss_fit_factor", "ss_lambda", "ss_status_string", "ss_stream_status",
 )
 
@@ -73,6 +74,8 @@ def load() -> ctypes.CDLL:
     mla = [P, P, P, I, I, I, I, I, F, F, I, P, P, U]
     lib.ss_attn_mla_decode.argtypes = mla + [P]
     lib.ss_attn_mla_decode_ex.argtypes = mla + [ctypes.POINTER(ss_debug_opts), P]
+    lib.ss_attn_mla_decode_paged.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, F, I, P, P, U,
+                                             ctypes.POINTER(ss_debug_opts), P]
     lib.ss_attn_mla_decode_workspace_size.argtypes = [I, I, I, I]
     lib.ss_attn_mla_decode_workspace_size.restype = U
     lib.ss_calibrate.argtypes = [ctypes.POINTER(ss_problem), F, ctypes.POINTER(F), ctypes.POINTER(F)]
@@ -85,7 +88,8 @@ def load() -> ctypes.CDLL:
     lib.ss_stream_status.argtypes = [P]
     for name in ("ss_attn_prefill", "ss_attn_prefill_ex", "ss_attn_decode", "ss_attn_decode_ex",
                  "ss_attn_decode_noalloc", "ss_attn_decode_paged", "ss_attn_mla_decode",
-                 "ss_attn_mla_decode_ex", "ss_calibrate", "ss_fit_factor", "ss_stream_status"):
+                 "ss_attn_mla_decode_ex", "ss_attn_mla_decode_paged", "ss_calibrate",
+                 "ss_fit_factor", "ss_stream_status"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -229,3 +233,17 @@ def ss_lambda(A, B, s, L) -> float:
 
 def ss_stream_status(stream=None) -> int:
     return load().ss_stream_status(_stream(stream))
+
+
+def ss_attn_mla_decode_paged(q, kv_pages, page_table, seq_lens, o, B, Hq, num_pages, max_pages,
+                             d_latent, d_rope, scale, lambda_a, num_kv_splits, skip_counts=None,
+                             workspace=None, workspace_bytes=0, skip_mask=None, vote_margin=None,
+                             count_only=False, stream=None) -> int:
+    """Latent-attention decode over a paged latent cache (pages of 128 rows)."""
+    dbg = _dbg(skip_mask, vote_margin, count_only)
+    return load().ss_attn_mla_decode_paged(_ptr(q), _ptr(kv_pages), _ptr(page_table),
+                                           _ptr(seq_lens), _ptr(o), B, Hq, num_pages, max_pages,
+                                           d_latent, d_rope, float(scale), float(lambda_a),
+                                           int(num_kv_splits), _ptr(skip_counts), _ptr(workspace),
+                                           int(workspace_bytes), ctypes.byref(dbg),
+                                           _stream(stream))

@@ -25,6 +25,15 @@ struct MlaParams {
   uint8_t* mask;           // [B][nT]
   float* margin;           // [B][nT]
   uint32_t* status;
+  // Paged latent cache (nullptr: contiguous [B][Lk][kMlaDk]).  Pages of one
+  // 128-key tile, [num_pages][128][kMlaDk]; page_table[b][j] is the page of
+  // sequence b's tile j, seq_lens[b] its length; each sequence has its own
+  // threshold lambda_b = min(1, lambda_a / seq_len) and its own split of its
+  // ceil(seq_len / 128) tiles.
+  const int32_t* page_table;
+  const int32_t* seq_lens;
+  int max_pages;
+  float lambda_a;
 };
 
 cudaError_t launch_mla_decode(const CUtensorMap& tkv, const MlaParams& p, Mode mode,

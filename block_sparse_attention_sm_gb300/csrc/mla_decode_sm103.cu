@@ -139,16 +139,35 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
   const int G = p.Hq;
   const int split = blockIdx.x % p.S;
   const int b = blockIdx.x / p.S;
-  const int j0 = split * p.T;
-  const int nt = max(0, min(p.nT, j0 + p.T) - j0);
-  auto tile_rows = [&](int t) { return min(kTile, p.Lk - (j0 + t) * kTile); };
+  // Sequence geometry: one length for the batch, or per sequence (paged).
+  const bool paged = p.page_table != nullptr;
+  int len = p.Lk, nT_b = p.nT, T_b = p.T, row_stride = p.nT;
+  float thr_raw = p.thr_raw;
+  if (paged) {
+    len = max(0, min(p.seq_lens[b], p.max_pages * kTile));
+    nT_b = (len + kTile - 1) / kTile;
+    T_b = (nT_b + p.S - 1) / p.S;
+    row_stride = p.max_pages;
+    // lambda_b = min(1, a / L_b) ("Skip-Softmax" §The threshold); a = 0: dense
+    thr_raw = (p.lambda_a > 0.f && len > 0)
+                  ? logf(fminf(1.f, p.lambda_a / static_cast<float>(len))) / p.scale
+                  : -INFINITY;
+  }
+  const int j0 = split * T_b;
+  const int nt = max(0, min(nT_b, j0 + T_b) - j0);
+  auto tile_rows = [&](int t) { return min(kTile, len - (j0 + t) * kTile); };
+  // Tensor-map coordinates (row, outer) of the split's tile t.
+  auto tile_y = [&](int t) { return paged ? 0 : (j0 + t) * kTile; };
+  auto tile_z = [&](int t) {
+    return paged ? p.page_table[static_cast<long>(b) * p.max_pages + j0 + t] : b;
+  };
 
   // ------------------------------------------------------------------ setup
   int n_k = 0;  // key-chunk copies issued (teardown bookkeeping)
   auto issue_chunk = [&](int e) {  // copy e = kChunks * t + c of the split's key stream
     const int t = e / kChunks, c = e - (e / kChunks) * kChunks, st = e % NKB;
     mbar_arrive_expect_tx(&ctl->kb_full[st], C::kChunkBytes);
-    tma_load_3d(sK + st * C::kChunkBytes, &tmKV, &ctl->kb_full[st], 64 * c, (j0 + t) * kTile, b);
+    tma_load_3d(sK + st * C::kChunkBytes, &tmKV, &ctl->kb_full[st], 64 * c, tile_y(t), tile_z(t));
     n_k = e + 1;
   };
   if (warp == kWarpK && lane == 0) {
@@ -232,8 +251,8 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
             }
             mbar_arrive_expect_tx(&ctl->vp_full[vs], C::kPairBytes);
             uint8_t* dst = sV + vs * C::kPairBytes;
-            tma_load_3d(dst, &tmKV, &ctl->vp_full[vs], 128 * c, (j0 + t) * kTile, b);
-            tma_load_3d(dst + 16384, &tmKV, &ctl->vp_full[vs], 128 * c + 64, (j0 + t) * kTile, b);
+            tma_load_3d(dst, &tmKV, &ctl->vp_full[vs], 128 * c, tile_y(t), tile_z(t));
+            tma_load_3d(dst + 16384, &tmKV, &ctl->vp_full[vs], 128 * c + 64, tile_y(t), tile_z(t));
             n_v = f + 1;
           }
         }
@@ -271,38 +290,58 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       }
     } else if (warp == kWarpPV) {
       // ---------------------------------------------------------- value MMAs
-      if (kPV && lane == 0 && nt > 0) {
+      // The whole warp runs the loop (it zeroes the rows of a partial page);
+      // lane 0 issues the MMAs and commits.
+      if (kPV && nt > 0) {
         constexpr uint32_t idO = idesc_bf16_f32(128, NQ, true, false);
         const uint32_t sVa = smem_u32(sV), sPa = smem_u32(sP);
         bool fine = true;
         for (int i = 0; fine; ++i) {
           const int s = i % NV;
-          if (!mbar_wait(&ctl->p_full[s], (i / NV) & 1, abort_flag)) break;
+          if (!__all_sync(0xffffffffu, mbar_wait(&ctl->p_full[s], (i / NV) & 1, abort_flag))) break;
           if (*reinterpret_cast<volatile int*>(&ctl->prec[s]) == 0) break;
+          // A page's rows past the sequence end hold whatever the cache holds
+          // (TMA fills only rows outside the tensor map with zeros): zero them
+          // so that P = 0 there cannot meet a non-finite value.
+          const int rows = paged ? tile_rows(*reinterpret_cast<volatile int*>(&ctl->kq[s])) : kTile;
           const uint64_t dp = smem_desc(sPa + s * C::kPBytes, 16, 1024);
           for (int c = 0; c < kPairs; ++c) {
             const int f = kPairs * i + c, vs = f % NVP;
-            if (!mbar_wait(&ctl->vp_full[vs], (f / NVP) & 1, abort_flag)) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&ctl->vp_full[vs], (f / NVP) & 1, abort_flag))) {
               fine = false;
               break;
             }
-            tc_fence_after();
-            // V_c^T: M = 128 latent entries (two 64-entry halves 16 KB
-            // apart), K = keys in 8-row groups of 1 KB.
-            const uint64_t dv = smem_desc(sVa + vs * C::kPairBytes, 16384, 1024);
-#pragma unroll
-            for (int kk = 0; kk < kTile / 16; ++kk) {
-              const uint32_t va = (kk * 2048) >> 4;
-              const uint32_t pa = ((kk >> 2) * NQ * 128 + (kk & 3) * 32) >> 4;
-              mma_bf16_ss(tmem + C::kColO + (kPairs * s + c) * NQ, dv + va, dp + pa, idO,
-                          kk > 0 ? 1u : 0u);
+            if (rows < kTile) {
+              uint4* base = reinterpret_cast<uint4*>(sV + vs * C::kPairBytes);
+              for (int idx = rows * 8 + lane; idx < kTile * 8; idx += 32) {
+                base[idx] = make_uint4(0u, 0u, 0u, 0u);         // latent entries 128c..+63
+                base[1024 + idx] = make_uint4(0u, 0u, 0u, 0u);  // latent entries 128c+64..+127
+              }
+              fence_proxy_async_smem();
             }
-            mma_commit(&ctl->vp_empty[vs]);
+            __syncwarp();
+            if (lane == 0) {
+              tc_fence_after();
+              // V_c^T: M = 128 latent entries (two 64-entry halves 16 KB
+              // apart), K = keys in 8-row groups of 1 KB.
+              const uint64_t dv = smem_desc(sVa + vs * C::kPairBytes, 16384, 1024);
+#pragma unroll
+              for (int kk = 0; kk < kTile / 16; ++kk) {
+                const uint32_t va = (kk * 2048) >> 4;
+                const uint32_t pa = ((kk >> 2) * NQ * 128 + (kk & 3) * 32) >> 4;
+                mma_bf16_ss(tmem + C::kColO + (kPairs * s + c) * NQ, dv + va, dp + pa, idO,
+                            kk > 0 ? 1u : 0u);
+              }
+              mma_commit(&ctl->vp_empty[vs]);
+            }
+            __syncwarp();
           }
-          if (fine) mma_commit(&ctl->slot_free[s]);
+          if (fine && lane == 0) mma_commit(&ctl->slot_free[s]);
         }
-        mma_commit(&ctl->pv_done);
-        mbar_wait(&ctl->pv_done, 0, nullptr);
+        if (lane == 0) {
+          mma_commit(&ctl->pv_done);
+          mbar_wait(&ctl->pv_done, 0, nullptr);
+        }
       }
     }
     if (lane == 0 && *abort_flag) {
@@ -395,9 +434,9 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       for (int g = 0; g < NQ; ++g)
         if (g < G && tm[g] != -INFINITY)
           cval = fmaxf(cval, (m[g] == -INFINITY) ? INFINITY : tm[g] - m[g]);
-      const bool skip = kVote && cval < p.thr_raw;
+      const bool skip = kVote && cval < thr_raw;
       if (tid == 0) {
-        const long gi = static_cast<long>(b) * p.nT + j0 + t;
+        const long gi = static_cast<long>(b) * row_stride + j0 + t;
         if (p.mask != nullptr) p.mask[gi] = skip ? 1 : 0;
         if (p.margin != nullptr) p.margin[gi] = (cval == INFINITY) ? INFINITY : cval * p.scale;
         skipped += skip ? 1u : 0u;
@@ -501,6 +540,12 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       }
     }
     if (tid == 0 && p.counts != nullptr) p.counts[static_cast<long>(b) * p.S + split] = skipped;
+    if (paged && split == 0 && tid < 32)
+      for (int j = nT_b + tid; j < p.max_pages; j += 32) {
+        const long gi = static_cast<long>(b) * row_stride + j;
+        if (p.mask != nullptr) p.mask[gi] = 2;
+        if (p.margin != nullptr) p.margin[gi] = NAN;
+      }
     tc_fence_before();
     __syncwarp();
   }

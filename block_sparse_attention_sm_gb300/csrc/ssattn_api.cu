@@ -353,6 +353,61 @@ ss_status ss_attn_decode(const void* q, const void* k_cache, const void* v_cache
                            num_kv_splits, skip_counts, workspace, workspace_bytes, nullptr, stream);
 }
 
+ss_status ss_attn_mla_decode_paged(const void* q, const void* kv_pages, const int32_t* page_table,
+                                   const int32_t* seq_lens, void* o, int B, int Hq, int num_pages,
+                                   int max_pages, int d_latent, int d_rope, float scale,
+                                   float lambda_a, int num_kv_splits, uint32_t* skip_counts,
+                                   void* workspace, size_t workspace_bytes,
+                                   const ss_debug_opts* dbg, void* stream) {
+  const bool count_only = dbg != nullptr && dbg->count_only != 0;
+  if (q == nullptr || kv_pages == nullptr || page_table == nullptr || seq_lens == nullptr ||
+      (o == nullptr && !count_only))
+    return SS_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kv_pages) || (o != nullptr && !aligned16(o)))
+    return SS_ERR_INVALID_ARG;
+  if (B < 1 || Hq < 1 || num_pages < 1 || max_pages < 1 || num_kv_splits < 1 || !scale_ok(scale) ||
+      !(lambda_a >= 0.f) || !std::isfinite(lambda_a))
+    return SS_ERR_INVALID_ARG;
+  if (d_latent != kMlaLatent || d_rope != kMlaRope || Hq > kMlaMaxHeads) return SS_ERR_UNSUPPORTED;
+  const int S = num_kv_splits;
+  if (static_cast<long>(B) * S > 0x7fffffffL) return SS_ERR_INVALID_ARG;
+  if (!count_only && S > 1) {
+    if (workspace == nullptr || !aligned16(workspace) ||
+        workspace_bytes < mla_ws(B, Hq, d_latent, S))
+      return SS_ERR_WORKSPACE;
+  }
+  ss_status st = check_device();
+  if (st != SS_OK) return st;
+  // [num_pages][128][576]: page p is "row block" p of the map; a page index
+  // outside the pool reads zeros (TMA out-of-bounds fill), never faults.
+  CUtensorMap tkv;
+  if (!make_map(&tkv, kv_pages, kMlaDk, kTile, num_pages)) return SS_ERR_CUDA;
+  MlaParams p{};
+  p.B = B;
+  p.Hq = Hq;
+  p.Lk = max_pages * kTile;
+  p.nT = max_pages;
+  p.S = S;
+  p.T = static_cast<int>(ceil_div(max_pages, S));
+  p.scale = scale;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.thr_raw = -INFINITY;  // per sequence from lambda_a (in the kernel)
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.part = static_cast<float*>(workspace);
+  p.counts = skip_counts;
+  p.mask = dbg ? dbg->skip_mask : nullptr;
+  p.margin = dbg ? dbg->vote_margin : nullptr;
+  p.status = status_ptr();
+  p.page_table = page_table;
+  p.seq_lens = seq_lens;
+  p.max_pages = max_pages;
+  p.lambda_a = lambda_a;
+  const Mode mode = count_only ? Mode::kCount : (lambda_a == 0.f ? Mode::kDense : Mode::kSparse);
+  cudaError_t e = launch_mla_decode(tkv, p, mode, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? SS_OK : SS_ERR_CUDA;
+}
+
 size_t ss_attn_mla_decode_workspace_size(int B, int Hq, int d_latent, int num_kv_splits) {
   return mla_ws(B, Hq, d_latent, num_kv_splits);
 }

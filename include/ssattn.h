@@ -256,6 +256,37 @@ ss_status ss_attn_mla_decode_ex(const void* q, const void* kv, void* o, int B, i
                                 int num_kv_splits, uint32_t* skip_counts, void* workspace,
                                 size_t workspace_bytes, const ss_debug_opts* dbg, void* stream);
 
+/*
+ * Latent-attention decode over a paged, variable-length latent cache: the
+ * computation of ss_attn_mla_decode per sequence, with the layout and the
+ * per-sequence rules of ss_attn_decode_paged.
+ *   kv_pages:   [num_pages][128][d_latent + d_rope] bf16, one 128-key tile per
+ *               page (rows past a sequence's end in its last page are ignored).
+ *   page_table: [B][max_pages] int32 device array; entry j of sequence b is the
+ *               page of its keys [128 j, 128 j + 128).  Only the first
+ *               ceil(seq_lens[b] / 128) entries of a row are read.
+ *   seq_lens:   [B] int32 device array, keys per sequence (0 <= L_b <=
+ *               128 * max_pages; a zero-length sequence gives zeros).
+ *   lambda_a:   the a of lambda_b = min(1, a / L_b) ("Skip-Softmax" §The
+ *               threshold: threshold = factor / seqlen), per sequence; 0 =
+ *               dense.
+ *   num_kv_splits: each sequence's tiles in that many contiguous ranges of
+ *               ceil(tiles_b / num_kv_splits) tiles.
+ *   skip_counts: nullable, [B*num_kv_splits]; workspace as in
+ *               ss_attn_mla_decode.
+ *   dbg:        nullable; skip_mask / vote_margin are [B][max_pages] (tiles past
+ *               a sequence's end are marked not evaluated).
+ * Returns SS_OK, SS_ERR_INVALID_ARG (null pointer, misalignment, B, Hq,
+ * num_pages, max_pages or num_kv_splits < 1, scale <= 0, lambda_a < 0 or not
+ * finite), SS_ERR_UNSUPPORTED, SS_ERR_WORKSPACE or SS_ERR_CUDA.
+ */
+ss_status ss_attn_mla_decode_paged(const void* q, const void* kv_pages, const int32_t* page_table,
+                                   const int32_t* seq_lens, void* o, int B, int Hq, int num_pages,
+                                   int max_pages, int d_latent, int d_rope, float scale,
+                                   float lambda_a, int num_kv_splits, uint32_t* skip_counts,
+                                   void* workspace, size_t workspace_bytes,
+                                   const ss_debug_opts* dbg, void* stream);
+
 /* A calibration problem: the inputs the threshold is fitted on. */
 typedef enum { SS_PREFILL = 0, SS_DECODE = 1, SS_MLA_DECODE = 2 } ss_kind;
 typedef struct {

@@ -150,6 +150,29 @@ def test_mla_decode_rejects_before_launch(capi, kw, expect):
     assert st == getattr(capi, expect)
 
 
+@pytest.mark.parametrize("kw,expect", [
+    (dict(table=None), "SS_ERR_INVALID_ARG"),
+    (dict(lens=None), "SS_ERR_INVALID_ARG"),
+    (dict(num_pages=0), "SS_ERR_INVALID_ARG"),
+    (dict(max_pages=0), "SS_ERR_INVALID_ARG"),
+    (dict(a=-1.0), "SS_ERR_INVALID_ARG"),
+    (dict(a=float("inf")), "SS_ERR_INVALID_ARG"),
+    (dict(kv=FAKE + 4), "SS_ERR_INVALID_ARG"),
+    (dict(Hq=17), "SS_ERR_UNSUPPORTED"),
+    (dict(d_rope=32), "SS_ERR_UNSUPPORTED"),
+    (dict(S=4, ws=None), "SS_ERR_WORKSPACE"),
+])
+def test_mla_paged_decode_rejects_before_launch(capi, kw, expect):
+    args = dict(kv=FAKE, table=FAKE, lens=FAKE, Hq=16, num_pages=10, max_pages=4, d_rope=64,
+                a=1.0, S=1, ws=FAKE, ws_bytes=1 << 30)
+    args.update(kw)
+    st = capi.ss_attn_mla_decode_paged(FAKE, args["kv"], args["table"], args["lens"], FAKE, 2,
+                                       args["Hq"], args["num_pages"], args["max_pages"], 512,
+                                       args["d_rope"], 0.07, args["a"], args["S"], None,
+                                       args["ws"], args["ws_bytes"], stream=0)
+    assert st == getattr(capi, expect)
+
+
 def test_mla_calibration_problem_checks(capi):
     """A latent-attention calibration problem must have one KV head and the
     576-entry key width; checked before anything runs."""

@@ -111,3 +111,85 @@ def test_mla_full_size_sampled():
     units = sorted({0, cfg["B"] - 1, *rng.choice(cfg["B"], size=2, replace=False).tolist()})
     check_mla(inp.q, inp.kv, scale=cfg["scale"], lam=min(1.0, a / cfg["Lk"]),
               num_splits=cfg["num_splits"], units=units)
+
+
+def check_mla_paged(q, kv, lens, *, a, num_splits, spare_pages=3, seed=0):
+    """Scatter each sequence's rows into shuffled pages of 128 (NaN in every
+    unused page and in the rows past a sequence's end) and compare each
+    sequence with the oracle on its own rows."""
+    import oracle
+    from _parity import check_output, compare_decisions
+    from block_sparse_attention_sm_gb300 import capi
+
+    B, Hq, dk = q.shape
+    S = num_splits
+    n_used = sum(-(-L // 128) for L in lens)
+    num_pages = n_used + spare_pages
+    max_pages = max(1, max(-(-L // 128) for L in lens))
+    rng = np.random.default_rng(seed)
+    phys = rng.permutation(num_pages)
+    pages = torch.full((num_pages, 128, dk), float("nan"), dtype=kv.dtype, device=kv.device)
+    table = np.full((B, max_pages), int(phys[0]), dtype=np.int32)
+    nxt = 0
+    for b, L in enumerate(lens):
+        for j in range(-(-L // 128)):
+            pg = int(phys[nxt])
+            nxt += 1
+            rows = min(128, L - 128 * j)
+            pages[pg, :rows] = kv[b, 128 * j:128 * j + rows]
+            table[b, j] = pg
+    table_t = torch.from_numpy(table).to(q.device)
+    lens_t = torch.tensor(lens, dtype=torch.int32, device=q.device)
+    ws_n = capi.ss_attn_mla_decode_workspace_size(B, Hq, 512, S)
+    ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=q.device)
+    o = torch.full((B, Hq, 512), float("nan"), dtype=q.dtype, device=q.device)
+    counts = torch.full((B * S,), -1, dtype=torch.int32, device=q.device)
+    mask = torch.full((B, max_pages), 7, dtype=torch.uint8, device=q.device)
+    margin = torch.full((B, max_pages), 12345.0, dtype=torch.float32, device=q.device)
+    st = capi.ss_attn_mla_decode_paged(q, pages, table_t, lens_t, o, B, Hq, num_pages, max_pages,
+                                       512, dk - 512, SCALE, a, S, counts, ws, ws_n, mask, margin)
+    assert st == capi.SS_OK, capi.ss_status_string(st)
+    assert capi.ss_stream_status() == capi.SS_OK
+    torch.cuda.synchronize()
+    og = o.float().cpu().numpy()
+    mh, gh = mask.cpu().numpy(), margin.cpu().numpy()
+    ch = counts.cpu().numpy().reshape(B, S)
+    for b, L in enumerate(lens):
+        nT = -(-L // 128)
+        assert (mh[b, nT:] == 2).all(), "tiles past the sequence end must be 'not evaluated'"
+        if L == 0:
+            assert (ch[b] == 0).all()
+            np.testing.assert_array_equal(og[b], 0.0)
+            continue
+        lam = min(1.0, a / L) if a > 0 else 0.0
+        T = -(-nT // S)
+        qs, kvs = q[b:b + 1], kv[b:b + 1, :L]
+        ref = oracle.mla_decode(qs, kvs, d_latent=512, scale=SCALE, lam=lam, num_splits=S)
+        _, row_dis = compare_decisions(mh[b:b + 1, :nT], gh[b:b + 1, :nT], ref.mask, ref.margin, lam)
+        for sp in range(S):
+            tiles = list(range(sp * T, min(nT, sp * T + T)))
+            assert ch[b, sp] == (int((mh[b, tiles] == 1).sum()) if tiles else 0)
+            if not row_dis[0]:
+                assert ch[b, sp] == ref.counts[0, sp]
+        over = oracle.mla_decode(qs, kvs, d_latent=512, scale=SCALE, lam=lam, num_splits=S,
+                                 mask_override=(mh[b:b + 1, :nT] == 1).astype(np.uint8))
+        check_output(og[b], over.o[0], f"paged mla sequence {b} under GPU mask")
+        if not row_dis[0]:
+            check_output(og[b], ref.o[0], f"paged mla sequence {b}")
+
+
+PAGED = [
+    # B, Hq, lens, splits
+    (4, 16, [1000, 0, 129, 3000], 3),   # ragged, an empty sequence, one row past a page
+    (3, 12, [128, 5000, 1], 2),
+    (2, 16, [4096, 2500], 1),
+]
+
+
+@pytest.mark.parametrize("case", PAGED)
+@pytest.mark.parametrize("a", [0.0, 1.0, 8.0])
+def test_mla_paged(case, a):
+    B, Hq, lens, S = case
+    Lmax = max(128, -(-max(lens) // 128) * 128)
+    inp = _inputs(B, Hq, Lmax, seed=6)
+    check_mla_paged(inp.q, inp.kv, lens, a=a, num_splits=S, seed=4)
