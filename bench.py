@@ -592,7 +592,7 @@ def run_suite(args):
         calibrated for 70% on the contiguous 32K cache of the same data."""
         from block_sparse_attention_sm_gb300 import capi
 
-        B, Hq, S, Lmax = 128, 16, 4, 32768
+        B, Hq, S, Lmax = (args.mla_batch or 128), 16, 4, 32768
         rng = np.random.default_rng(9)
         lens = [int(x) for x in rng.integers(8192, Lmax + 1, size=B)]
         inp = synth.mla_decode_inputs(B=B, Hq=Hq, Lk=Lmax, hot_frac=0.10, seed=0, device=dev)
@@ -845,7 +845,7 @@ def main():
     ap.add_argument("--decode-batch", type=int, default=0,
                     help="profiling: shrink the decode workload to this many sequences")
     ap.add_argument("--mla-batch", type=int, default=0,
-                    help="profiling: shrink the latent-attention suite workload to this many sequences")
+                    help="profiling: shrink the latent-attention suite workloads to this many sequences")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
