@@ -702,6 +702,7 @@ def run_suite(args):
     if "prefill" in parts:
         prefill_points("tiny_prefill", [0.0, 0.5, 0.75])
         prefill_points("dit_prefill_32k", [0.0, 0.5, 0.7])
+        prefill_points("dit_prefill_32k_d64", [0.0, 0.5, 0.7])
         prefill_points("llama_prefill_16k", [0.0, 0.5, 0.7])
     if "chunked" in parts:
         prefill_points("llama_chunked_prefill_2k_on_32k", [0.0, 0.5, 0.7, 0.9])

@@ -157,6 +157,9 @@ WORKLOADS = {
                          scale=1.0 / 8.0, hot_frac=0.20, per_head_u=False),
     "dit_prefill_32k": dict(kind="prefill", B=1, Hq=24, Hkv=24, Lq=32768, Lk=32768, d=128,
                             causal=False, scale=128 ** -0.5, hot_frac=0.15, per_head_u=False),
+    # the DiT shape with 64-wide heads
+    "dit_prefill_32k_d64": dict(kind="prefill", B=1, Hq=24, Hkv=24, Lq=32768, Lk=32768, d=64,
+                                causal=False, scale=64 ** -0.5, hot_frac=0.15, per_head_u=False),
     "llama_prefill_16k": dict(kind="prefill", B=1, Hq=32, Hkv=8, Lq=16384, Lk=16384, d=128,
                               causal=True, scale=128 ** -0.5, hot_frac=0.10, per_head_u=True),
     "llama_decode_32k": dict(kind="decode", B=64, Hq=32, Hkv=8, Lk=32768, d=128,
