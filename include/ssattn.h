@@ -127,7 +127,8 @@ size_t ss_attn_decode_workspace_size(int B, int Hq, int d, int num_kv_splits);
  * ceil(nT/num_kv_splits) tiles; each range runs its own online pass (its
  * first tile is always kept), streams all of its K, loads V only for kept
  * tiles, and writes a partial (m, l, O); a second kernel merges the
- * partials by log-sum-exp into bf16 o.
+ * partials by log-sum-exp into bf16 o.  The G = Hq/Hkv query heads of a KV
+ * head vote together on each tile; G <= 32 (SS_ERR_UNSUPPORTED above).
  *   skip_counts: nullable device buffer [B*Hkv*num_kv_splits] (skipped tiles
  *     per (sequence, KV head, split)); overwritten.
  *   workspace: device buffer of at least
