@@ -178,6 +178,36 @@ def test_decisions_equal_prefix_max_form(oracle_lib, shape):
         prev_mask = res.mask.copy()
 
 
+@pytest.mark.parametrize("shape", [(1, 2, 1, 16, 24, 8, False, 4, 4),
+                                   (1, 1, 1, 13, 13, 5, True, 4, 4)])
+def test_every_critical_value_sweep(oracle_lib, shape):
+    """lambda at every midpoint between consecutive critical values (and
+    below / above all of them): by property P a tile is skipped exactly when
+    its statistic c_j < ln(lambda), so the launch skips exactly the number of
+    critical values below ln(lambda), and the skipped sets are nested."""
+    B, Hq, Hkv, Lq, Lk, d, causal, Bq, Bk = shape
+    nT = -(-Lk // Bk)
+    (q, k, v, scale), res0 = run_prefill_case(oracle_lib, shape, 0.0, 5, hot=True)
+    cs = []
+    for u in res0.units:
+        s, _ = unit_scores(q, k, scale, shape, u)
+        _, c = prefix_decisions(s, Bk, range(nT), -np.inf)
+        cs.extend(x for x in c if np.isfinite(x))
+    cs = np.sort(np.array(cs))
+    below_zero = np.unique(cs[cs < 0])
+    assert len(below_zero) >= 3, "the case must have several critical values below ln 1"
+    pts = np.concatenate([[below_zero[0] - 1.0], (below_zero[:-1] + below_zero[1:]) / 2, [0.0]])
+    prev = None
+    for x in pts:
+        lam = float(np.exp(x))
+        _, res = run_prefill_case(oracle_lib, shape, lam, 5, hot=True)
+        skipped = int(res.counts.sum())
+        assert skipped == int((cs < math.log(lam)).sum())
+        if prev is not None:
+            assert ((prev == 1) <= (res.mask == 1)).all()
+        prev = res.mask.copy()
+
+
 @pytest.mark.parametrize("shape", PREFILL_SHAPES[:6])
 @pytest.mark.parametrize("lam", [0.02, 0.2, 0.6])
 def test_sparse_output_is_softmax_over_kept_tiles(oracle_lib, shape, lam):
