@@ -1,6 +1,7 @@
 // Internal declarations of the latent-attention (MLA) decode kernel.
 #pragma once
 #include "common.cuh"
+#include "ptx_sm103.cuh"
 
 namespace ssattn {
 
@@ -10,7 +11,8 @@ namespace ssattn {
 constexpr int kMlaLatent = 512;
 constexpr int kMlaRope = 64;
 constexpr int kMlaDk = kMlaLatent + kMlaRope;
-constexpr int kMlaMaxHeads = 16;  // voting group = MMA N of at most 16 rows
+constexpr int kMlaNarrowHeads = 16;  // one softmax warpgroup (MMA N = 16) up to here
+constexpr int kMlaMaxHeads = 32;     // two softmax warpgroups (MMA N = 32)
 
 struct MlaParams {
   int B, Hq, Lk;
@@ -38,5 +40,36 @@ struct MlaParams {
 
 cudaError_t launch_mla_decode(const CUtensorMap& tkv, const MlaParams& p, Mode mode,
                               cudaStream_t st);
+// Heads 17..32: the wide kernel (two softmax warpgroups of 16 heads each).
+cudaError_t launch_mla_decode_wide(const CUtensorMap& tkv, const MlaParams& p, Mode mode,
+                                   cudaStream_t st);
+// Log-sum-exp merge of the S > 1 partial states in p.part into p.o.
+cudaError_t launch_mla_merge(const MlaParams& p, cudaStream_t st);
+
+// tcgen05.ld of 16 consecutive fp32 columns of the warp's 32 lanes.
+__device__ __forceinline__ void mla_tmem_ld16(uint32_t taddr, float (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=f"(r[0]), "=f"(r[1]), "=f"(r[2]), "=f"(r[3]), "=f"(r[4]), "=f"(r[5]), "=f"(r[6]),
+        "=f"(r[7]), "=f"(r[8]), "=f"(r[9]), "=f"(r[10]), "=f"(r[11]), "=f"(r[12]), "=f"(r[13]),
+        "=f"(r[14]), "=f"(r[15])
+      : "r"(taddr));
+}
+
+// Wait (bounded, no abort flag) for the newest copy issued into each slot of
+// a ring of N slots after n copies: the slot of copy i is i % N.
+template <int N>
+__device__ __forceinline__ void mla_drain_ring(uint64_t* full, int n) {
+  for (int s = 0; s < N; ++s)
+    if (n > s) mbar_wait(&full[s], ((((n - 1 - s) / N) * N + s) / N) & 1, nullptr);
+}
+
+// Maximum over the warp (every lane gets it).
+__device__ __forceinline__ float mla_warp_max(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
 
 }  // namespace ssattn

@@ -48,6 +48,9 @@ namespace {
 constexpr int kMlaThreads = 256;
 constexpr int kWarpK = 4, kWarpV = 5, kWarpS = 6, kWarpPV = 7;
 
+// Ring depths, the same for every mode: at 16 heads the voting kernel with
+// two value slots and seven or eight key slots measured 3-4% slower.
+template <Mode MODE>
 struct MlaCfg {
   static constexpr int NQ = 16;          // MMA N (heads padded with zero rows)
   static constexpr int NKB = 6;          // key-chunk slots (64 entries x 128 keys)
@@ -76,51 +79,29 @@ struct MlaCfg {
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
 
+template <Mode MODE>
 struct MlaCtl {
-  uint64_t kb_full[MlaCfg::NKB], kb_empty[MlaCfg::NKB];
-  uint64_t vp_full[MlaCfg::NVP], vp_empty[MlaCfg::NVP];
-  uint64_t s_full[MlaCfg::NS], s_empty[MlaCfg::NS];
-  uint64_t vq_full[MlaCfg::NV], p_full[MlaCfg::NV], slot_free[MlaCfg::NV];
+  using C = MlaCfg<MODE>;
+  uint64_t kb_full[C::NKB], kb_empty[C::NKB];
+  uint64_t vp_full[C::NVP], vp_empty[C::NVP];
+  uint64_t s_full[C::NS], s_empty[C::NS];
+  uint64_t vq_full[C::NV], p_full[C::NV], slot_free[C::NV];
   uint64_t s_done, pv_done;
-  int kq[MlaCfg::NV];     // kept tile for the value producer (-1: no more)
-  int prec[MlaCfg::NV];   // 1: P written, 0: no more (value-MMA issuer)
+  int kq[C::NV];     // kept tile for the value producer (-1: no more)
+  int prec[C::NV];   // 1: P written, 0: no more (value-MMA issuer)
   uint32_t tmem_base;
   int abort_flag;
 };
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-      : "=f"(r[0]), "=f"(r[1]), "=f"(r[2]), "=f"(r[3]), "=f"(r[4]), "=f"(r[5]), "=f"(r[6]),
-        "=f"(r[7]), "=f"(r[8]), "=f"(r[9]), "=f"(r[10]), "=f"(r[11]), "=f"(r[12]), "=f"(r[13]),
-        "=f"(r[14]), "=f"(r[15])
-      : "r"(taddr));
-}
-
-__device__ __forceinline__ float warp_max32(float v) {
-  float r;
-  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
-  return r;
-}
-
-// Wait (bounded, no abort flag) for the newest copy issued into each slot of
-// a ring of N slots after n copies: the slot of copy i is i % N.
-template <int N>
-__device__ __forceinline__ void drain_ring(uint64_t* full, int n) {
-  for (int s = 0; s < N; ++s)
-    if (n > s) mbar_wait(&full[s], ((((n - 1 - s) / N) * N + s) / N) & 1, nullptr);
-}
-
 template <Mode MODE>
 __global__ void __launch_bounds__(kMlaThreads, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tmKV, const MlaParams p) {
-  using C = MlaCfg;
+  using C = MlaCfg<MODE>;
   constexpr int NQ = C::NQ, NKB = C::NKB, NVP = C::NVP, NS = C::NS, NV = C::NV;
   constexpr int kChunks = C::kChunks, kPairs = C::kPairs;
   constexpr bool kPV = (MODE != Mode::kCount);
   constexpr bool kVote = (MODE != Mode::kDense);
-  static_assert(sizeof(MlaCtl) <= C::kCtlBytes, "control block overflow");
+  static_assert(sizeof(MlaCtl<MODE>) <= C::kCtlBytes, "control block overflow");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -132,7 +113,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
   float* sRed = reinterpret_cast<float*>(smem + C::kRedOff);
   float* sLRed = reinterpret_cast<float*>(smem + C::kLRedOff);
   float* sMs = reinterpret_cast<float*>(smem + C::kMsOff);
-  auto* ctl = reinterpret_cast<MlaCtl*>(smem + C::kCtlOff);
+  auto* ctl = reinterpret_cast<MlaCtl<MODE>*>(smem + C::kCtlOff);
   volatile int* abort_flag = &ctl->abort_flag;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -346,8 +327,8 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     }
     if (lane == 0 && *abort_flag) {
       // Let in-flight copies land before shared memory is released.
-      if (warp == kWarpK) drain_ring<NKB>(ctl->kb_full, n_k);
-      if (warp == kWarpV) drain_ring<NVP>(ctl->vp_full, n_v);
+      if (warp == kWarpK) mla_drain_ring<NKB>(ctl->kb_full, n_k);
+      if (warp == kWarpV) mla_drain_ring<NVP>(ctl->vp_full, n_v);
     }
     __syncwarp();
   } else {
@@ -385,7 +366,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
 #pragma unroll
       for (int c = 0; c < kPairs; ++c) {
         float o[NQ];
-        tmem_ld16(lane_base + C::kColO + (kPairs * (j % NV) + c) * NQ, o);
+        mla_tmem_ld16(lane_base + C::kColO + (kPairs * (j % NV) + c) * NQ, o);
         tmem_wait_ld();
 #pragma unroll
         for (int g = 0; g < NQ; ++g) acc[c][g] = fmaf(acc[c][g], f[g], o[g]);
@@ -399,7 +380,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       tc_fence_after();
       float s[NQ];
       if (got) {
-        tmem_ld16(lane_base + C::kColS + NQ * sb, s);
+        mla_tmem_ld16(lane_base + C::kColS + NQ * sb, s);
         tmem_wait_ld();
       }
       tc_fence_before();
@@ -416,7 +397,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       float mine = -INFINITY;
 #pragma unroll
       for (int g = 0; g < NQ; ++g) {
-        const float wm = warp_max32(s[g]);
+        const float wm = mla_warp_max(s[g]);
         if (lane == g) mine = wm;
       }
       if (lane < NQ) sRed[((t & 1) * NQ + lane) * 4 + warp] = mine;
@@ -594,18 +575,22 @@ template <Mode MODE>
 cudaError_t launch_mla(const CUtensorMap& tkv, const MlaParams& p, cudaStream_t st) {
   auto* fn = mla_decode_kernel<MODE>;
   cudaError_t e =
-      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, MlaCfg::kSmemBytes);
+      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, MlaCfg<MODE>::kSmemBytes);
   if (e != cudaSuccess) return e;
   const long ctas = static_cast<long>(p.B) * p.S;
-  fn<<<dim3(static_cast<unsigned>(ctas)), dim3(kMlaThreads), MlaCfg::kSmemBytes, st>>>(tkv, p);
+  fn<<<dim3(static_cast<unsigned>(ctas)), dim3(kMlaThreads), MlaCfg<MODE>::kSmemBytes, st>>>(tkv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess || MODE == Mode::kCount || p.S == 1) return e;
+  return launch_mla_merge(p, st);
+}
+
+}  // namespace
+
+cudaError_t launch_mla_merge(const MlaParams& p, cudaStream_t st) {
   const int rows = p.B * p.Hq;
   mla_merge_kernel<<<dim3((rows + 7) / 8), dim3(256), 0, st>>>(p.part, p.o, rows, p.S);
   return cudaGetLastError();
 }
-
-}  // namespace
 
 cudaError_t launch_mla_decode(const CUtensorMap& tkv, const MlaParams& p, Mode mode,
                               cudaStream_t st) {

@@ -247,7 +247,9 @@ ss_status mla_impl(const void* q, const void* kv, void* o, int B, int Hq, int Lk
   p.margin = dbg ? dbg->vote_margin : nullptr;
   p.status = status_ptr();
   const Mode mode = count_only ? Mode::kCount : (dense ? Mode::kDense : Mode::kSparse);
-  cudaError_t e = launch_mla_decode(tkv, p, mode, static_cast<cudaStream_t>(stream));
+  cudaError_t e = (Hq > kMlaNarrowHeads)
+                      ? launch_mla_decode_wide(tkv, p, mode, static_cast<cudaStream_t>(stream))
+                      : launch_mla_decode(tkv, p, mode, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
@@ -404,7 +406,9 @@ ss_status ss_attn_mla_decode_paged(const void* q, const void* kv_pages, const in
   p.max_pages = max_pages;
   p.lambda_a = lambda_a;
   const Mode mode = count_only ? Mode::kCount : (lambda_a == 0.f ? Mode::kDense : Mode::kSparse);
-  cudaError_t e = launch_mla_decode(tkv, p, mode, static_cast<cudaStream_t>(stream));
+  cudaError_t e = (Hq > kMlaNarrowHeads)
+                      ? launch_mla_decode_wide(tkv, p, mode, static_cast<cudaStream_t>(stream))
+                      : launch_mla_decode(tkv, p, mode, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 

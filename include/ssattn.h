@@ -61,7 +61,7 @@ typedef enum {
   SS_OK = 0,
   SS_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad shape, lambda or scale */
   SS_ERR_UNSUPPORTED = 2,  /* d not in {64,128}, decode with Hq/Hkv > 32, latent decode
-                              with other widths or Hq > 16, or the current device is not
+                              with other widths or Hq > 32, or the current device is not
                               sm_103 */
   SS_ERR_CUDA = 3,         /* a CUDA runtime call failed (launch, copy, sync) */
   SS_ERR_TIMEOUT = 4,      /* a kernel's bounded wait expired (logic error; reported, not hung) */
@@ -234,7 +234,8 @@ ss_status ss_attn_decode_noalloc(const void* q, const void* k_cache, const void*
  *   q:  [B][Hq][dk] bf16 (the absorbed queries), 16-byte aligned.
  *   kv: [B][Lk][dk] bf16 latent cache, contiguous, 16-byte aligned.
  *   o:  [B][Hq][d_latent] bf16.
- *   Only d_latent = 512, d_rope = 64 and 1 <= Hq <= 16 are supported.
+ *   Only d_latent = 512, d_rope = 64 and 1 <= Hq <= 32 are supported (up to
+ *   16 heads take one softmax warpgroup, 17..32 heads two).
  *   skip_counts: nullable device buffer [B*num_kv_splits]; overwritten.
  *   workspace: device buffer of at least
  *     ss_attn_mla_decode_workspace_size(B, Hq, d_latent, num_kv_splits)

@@ -73,7 +73,7 @@ def test_mla_random_shapes(seed):
 
     rng = np.random.default_rng(3000 + seed)
     B = int(rng.integers(1, 4))
-    Hq = int(rng.integers(1, 17))
+    Hq = int(rng.integers(1, 33))
     Lk = int(rng.integers(1, 6000))
     S = int(rng.integers(1, 7))
     inp = synth.mla_decode_inputs(B=B, Hq=Hq, Lk=Lk, hot_frac=float(rng.uniform(0.05, 0.4)),

@@ -39,6 +39,11 @@ CASES = [
     (2, 12, 4096, 8),     # heads padded to the MMA's 16 rows
     (1, 16, 300, 5),      # more splits than tiles: empty splits
     (1, 16, 20000, 2),    # long splits: the copy ring wraps many times
+    # 17..32 heads: two softmax warpgroups of 16 heads each
+    (2, 17, 1000, 1),     # one head in the second warpgroup
+    (3, 24, 5000, 3),     # heads padded to the MMA's 32 rows
+    (2, 32, 4096, 8),     # both warpgroups full
+    (1, 32, 20000, 2),    # long splits
 ]
 
 
@@ -52,21 +57,23 @@ def test_mla_decode(case, a):
     check_mla(inp.q, inp.kv, scale=SCALE, lam=min(1.0, a / Lk), num_splits=S)
 
 
-def test_mla_random_scores_many_decisions():
+@pytest.mark.parametrize("Hq", [16, 32])
+def test_mla_random_scores_many_decisions(Hq):
     """Plain N(0,1) inputs: margins spread out around the threshold."""
     from _parity import check_mla
 
     g = torch.Generator(device="cuda").manual_seed(8)
-    q = torch.randn(2, 16, 576, device="cuda", generator=g).to(torch.bfloat16)
+    q = torch.randn(2, Hq, 576, device="cuda", generator=g).to(torch.bfloat16)
     kv = torch.randn(2, 3000, 576, device="cuda", generator=g).to(torch.bfloat16)
     for lam in (0.3, 0.8):
         check_mla(q, kv, scale=576 ** -0.5, lam=lam, num_splits=3)
 
 
-def test_mla_count_only_matches_the_full_launch():
+@pytest.mark.parametrize("Hq", [16, 32])
+def test_mla_count_only_matches_the_full_launch(Hq):
     from block_sparse_attention_sm_gb300 import capi
 
-    B, Hq, Lk, S = 4, 16, 8192, 4
+    B, Lk, S = 4, 8192, 4
     inp = _inputs(B, Hq, Lk, frac=0.1, seed=2)
     lam = 3.0 / Lk
     ws_n = capi.ss_attn_mla_decode_workspace_size(B, Hq, 512, S)
@@ -96,15 +103,16 @@ def test_mla_calibration_hits_the_target():
 
 
 @pytest.mark.slow
-def test_mla_full_size_sampled():
-    """The bench's workload (64 sequences x 32K keys, 16 splits) at lambda for
-    70% skipped tiles; the oracle checks the first, last and two random
-    sequences."""
+@pytest.mark.parametrize("name", ["mla_decode_32k", "mla_decode_32k_32h"])
+def test_mla_full_size_sampled(name):
+    """The bench's workloads (128 sequences x 32K keys, 4 splits, 16 or 32
+    heads) at lambda for 70% skipped tiles; the oracle checks the first, last
+    and two random sequences."""
     import block_sparse_attention_sm_gb300 as ss
     from _parity import check_mla
     from block_sparse_attention_sm_gb300 import synth
 
-    inp, cfg = synth.make("mla_decode_32k", seed=0, device="cuda")
+    inp, cfg = synth.make(name, seed=0, device="cuda")
     a, _ = ss.calibrate("mla_decode", inp.q, inp.kv, None, scale=cfg["scale"], target_sparsity=0.7,
                         num_kv_splits=cfg["num_splits"])
     rng = np.random.default_rng(3)
@@ -183,6 +191,8 @@ PAGED = [
     (4, 16, [1000, 0, 129, 3000], 3),   # ragged, an empty sequence, one row past a page
     (3, 12, [128, 5000, 1], 2),
     (2, 16, [4096, 2500], 1),
+    (3, 32, [1000, 0, 3000], 3),        # two softmax warpgroups
+    (2, 20, [129, 4096], 2),
 ]
 
 
