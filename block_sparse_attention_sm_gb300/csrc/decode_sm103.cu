@@ -7,15 +7,19 @@
 // V block is never loaded; the V tiles of kept tiles are fetched as soon as
 // the vote has decided, while the following K tiles keep streaming.
 //
-// One CTA = one (sequence b, KV head, split); 256 threads in 8 warps:
+// One CTA = one (sequence b, KV head, split); WG softmax warpgroups (one for
+// vote groups of up to 16 query rows, two above) and four role warps:
 //   warps 0-3  vote / softmax: thread i = TMEM lane i, which is key i of the
-//              tile for the scores and dimension i for the P.V result.
-//   warp 4     TMA producer of the K ring (NK stages, 128-byte swizzle).
-//   warp 5     TMA producer of the V slots (kept tiles only, in kept order).
-//   warp 6     TMEM allocator + issuer of the score MMAs
+//              tile for the scores and dimension i for the P.V result.  With
+//              two warpgroups, warps 0-3 keep rows 0-15 and warps 4-7 rows
+//              16-31, and each tile's vote takes two exchanges: the warp
+//              maxima of the rows, then each warpgroup's vote statistic.
+//   warp 4*WG  TMA producer of the K ring (NK stages, 128-byte swizzle).
+//   +1         TMA producer of the V slots (kept tiles only, in kept order).
+//   +2         TMEM allocator + issuer of the score MMAs
 //              S^T = K_tile . Q^T  (M = 128 keys, N = 16/32 query rows
 //              padded with zero rows, K = d), fp32 in TMEM.
-//   warp 7     issuer of the value MMAs  O_i^T = V_i^T . P_i^T
+//   +3         issuer of the value MMAs  O_i^T = V_i^T . P_i^T
 //              (M = 128 = d, N = query rows, K = 128 keys), one fresh TMEM
 //              accumulator per kept tile.
 // The G query heads that share the KV head (one token each) are the voting
@@ -37,8 +41,13 @@ namespace ssattn {
 
 namespace {
 
-constexpr int kDecThreads = 256;
-constexpr int kWarpK = 4, kWarpV = 5, kWarpS = 6, kWarpPV = 7;
+// Softmax warpgroups for a vote group padded to GP rows: one thread keeps the
+// state of GP / WG rows (with one warpgroup, 32 rows would sit at the
+// register cap and spill).
+template <int GP>
+constexpr int kDecWG = (GP > 16) ? 2 : 1;
+template <int GP>
+constexpr int kDecThreads = 128 * kDecWG<GP> + 128;
 
 template <int D, int GP>
 struct DecCfg {
@@ -59,7 +68,8 @@ struct DecCfg {
   static constexpr int kRedOff = kPOff + NV * kPBytes;            // float [2][GP][4]
   static constexpr int kLRedOff = kRedOff + 2 * GP * 4 * 4;       // float [GP][4]
   static constexpr int kMsOff = kLRedOff + GP * 4 * 4;            // float [2 NV][GP]
-  static constexpr int kCtlOff = (kMsOff + 2 * NV * GP * 4 + 15) / 16 * 16;
+  static constexpr int kPartOff = kMsOff + 2 * NV * GP * 4;       // float [2][2]
+  static constexpr int kCtlOff = (kPartOff + 16 + 15) / 16 * 16;
   static constexpr int kCtlBytes = 512;
   static constexpr int kSmemBytes = kCtlOff + kCtlBytes + 1024;  // + alignment slack
   static constexpr uint32_t kColS = 0;              // S buffer b at kColS + NQ b
@@ -119,12 +129,6 @@ __device__ __forceinline__ void tmem_ld_cols<16>(uint32_t taddr, float (&r)[16])
       : "r"(taddr));
 }
 
-template <>
-__device__ __forceinline__ void tmem_ld_cols<32>(uint32_t taddr, float (&r)[32]) {
-  tmem_ld_cols<16>(taddr, *reinterpret_cast<float(*)[16]>(&r[0]));
-  tmem_ld_cols<16>(taddr + 16, *reinterpret_cast<float(*)[16]>(&r[16]));
-}
-
 // Maximum over the warp (every lane gets it).
 __device__ __forceinline__ float warp_max(float v) {
   float r;
@@ -133,11 +137,13 @@ __device__ __forceinline__ float warp_max(float v) {
 }
 
 template <int D, int GP, Mode MODE>
-__global__ void __launch_bounds__(kDecThreads, 1)
+__global__ void __launch_bounds__(kDecThreads<GP>, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const DecodeParams p) {
   using C = DecCfg<D, GP>;
   constexpr int NK = C::NK, NV = C::NV, NS = C::NS, NQ = C::NQ;
+  constexpr int WG = kDecWG<GP>, HG = GP / WG;  // softmax warpgroups, rows per warpgroup
+  constexpr int kWarpK = 4 * WG, kWarpV = kWarpK + 1, kWarpS = kWarpK + 2;  // +3: value MMAs
   constexpr bool kPV = (MODE != Mode::kCount);
   constexpr bool kVote = (MODE != Mode::kDense);
   constexpr bool kDenseV = (MODE == Mode::kDense);  // every tile kept: V needs no decision
@@ -154,6 +160,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   float* sRed = reinterpret_cast<float*>(smem + C::kRedOff);
   float* sLRed = reinterpret_cast<float*>(smem + C::kLRedOff);
   float* sMs = reinterpret_cast<float*>(smem + C::kMsOff);
+  float* sPart = reinterpret_cast<float*>(smem + C::kPartOff);
   auto* ctl = reinterpret_cast<Ctl*>(smem + C::kCtlOff);
   volatile int* abort_flag = &ctl->abort_flag;
 
@@ -204,13 +211,13 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     }
     for (int s = 0; s < NS; ++s) {
       mbar_init(&ctl->s_full[s], 1);
-      mbar_init(&ctl->s_empty[s], 4);
+      mbar_init(&ctl->s_empty[s], 4 * WG);
     }
     for (int s = 0; s < NV; ++s) {
       mbar_init(&ctl->v_full[s], 1);
       mbar_init(&ctl->slot_free[s], 1);
       mbar_init(&ctl->vq_full[s], 1);
-      mbar_init(&ctl->p_full[s], 4);
+      mbar_init(&ctl->p_full[s], 4 * WG);
     }
     mbar_init(&ctl->s_done, 1);
     mbar_init(&ctl->pv_done, 1);
@@ -248,7 +255,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
 
-  if (warp >= 4) {
+  if (warp >= 4 * WG) {
     int n_v_issued = 0;
     if (warp == kWarpK) {
       // ---------------------------------------------------------- K producer
@@ -344,15 +351,19 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ vote / softmax
-    const int key = tid;  // TMEM lane: key of the tile (scores), dimension (P.V)
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const int wg = warp >> 2;   // softmax warpgroup: rows hg .. hg + HG - 1
+    const int hg = HG * wg;
+    const int wq = warp & 3;    // warp within the warpgroup
+    const int key = tid & 127;  // TMEM lane: key of the tile (scores), dimension (P.V)
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16) + hg;
+    constexpr int kSoftmaxThreads = 128 * WG;
     const float sl2 = p.scale_log2;
     auto wwait = [&](uint64_t* bar, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
     };
-    float m[GP], l[GP], acc[GP], macc[GP];
+    float m[HG], l[HG], acc[HG], macc[HG];
 #pragma unroll
-    for (int g = 0; g < GP; ++g) {
+    for (int g = 0; g < HG; ++g) {
       m[g] = -INFINITY;
       l[g] = 0.f;
       acc[g] = 0.f;
@@ -362,14 +373,14 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     int kept = 0;
     bool ok = true;
 
-    // Fold the P.V result of kept tile j (slot j % NV) into acc.
+    // Fold the P.V result of kept tile j (slot j % NV) into acc (own rows).
     auto accumulate = [&](int j) {
-      float o[GP];
-      tmem_ld_cols<GP>(lane_base + C::kColO + NQ * (j % NV), o);
+      float o[HG];
+      tmem_ld_cols<HG>(lane_base + C::kColO + NQ * (j % NV), o);
       tmem_wait_ld();
-      const float* ms = sMs + (j % (2 * NV)) * GP;
+      const float* ms = sMs + (j % (2 * NV)) * GP + hg;
 #pragma unroll
-      for (int g = 0; g < GP; ++g) {
+      for (int g = 0; g < HG; ++g) {
         const float mj = ms[g];
         const float f = (macc[g] == -INFINITY) ? 0.f : ex2_approx((macc[g] - mj) * sl2);
         acc[g] = fmaf(acc[g], f, o[g]);
@@ -382,9 +393,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       const bool got = wwait(&ctl->s_full[sb], (t / NS) & 1);
       ok = ok && got;
       tc_fence_after();
-      float s[GP];
+      float s[HG];
       if (got) {
-        tmem_ld_cols<GP>(lane_base + C::kColS + NQ * sb, s);
+        tmem_ld_cols<HG>(lane_base + C::kColS + NQ * sb, s);
         tmem_wait_ld();
       }
       tc_fence_before();
@@ -392,33 +403,41 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       if (lane == 0) mbar_arrive(&ctl->s_empty[sb]);
       const bool valid_key = got && key < tile_rows(t);
 #pragma unroll
-      for (int g = 0; g < GP; ++g)
+      for (int g = 0; g < HG; ++g)
         if (!valid_key) s[g] = -INFINITY;
 
       // Tile maximum of each row: warp maxima, exchanged through shared
-      // memory at one 128-thread barrier per tile (double-buffered by tile
-      // parity, so a warp that runs ahead cannot overwrite unread values).
+      // memory at one barrier of the softmax threads per tile (double-
+      // buffered by tile parity, so a warp that runs ahead cannot overwrite
+      // unread values).
       float mine = -INFINITY;
 #pragma unroll
-      for (int g = 0; g < GP; ++g) {
+      for (int g = 0; g < HG; ++g) {
         const float wm = warp_max(s[g]);
         if (lane == g) mine = wm;
       }
-      if (lane < GP) sRed[((t & 1) * GP + lane) * 4 + warp] = mine;
-      named_bar_sync(1, 128);
-      float tm[GP];
+      if (lane < HG) sRed[((t & 1) * GP + hg + lane) * 4 + wq] = mine;
+      named_bar_sync(1, kSoftmaxThreads);
+      float tm[HG];
 #pragma unroll
-      for (int g = 0; g < GP; ++g) {
-        const float4 r = *reinterpret_cast<const float4*>(sRed + ((t & 1) * GP + g) * 4);
+      for (int g = 0; g < HG; ++g) {
+        const float4 r = *reinterpret_cast<const float4*>(sRed + ((t & 1) * GP + hg + g) * 4);
         tm[g] = fmaxf(fmaxf(r.x, r.y), fmaxf(r.z, r.w));
       }
 
-      // Vote: skip iff every row r has tile_max_r - m_r < ln(lambda)/scale.
+      // Vote: skip iff every row r has tile_max_r - m_r < ln(lambda)/scale;
+      // with two warpgroups, each one's statistic over its rows, then the
+      // maximum of both (second barrier).
       float cval = -INFINITY;
 #pragma unroll
-      for (int g = 0; g < GP; ++g)
-        if (g < G && tm[g] != -INFINITY)
+      for (int g = 0; g < HG; ++g)
+        if (hg + g < G && tm[g] != -INFINITY)
           cval = fmaxf(cval, (m[g] == -INFINITY) ? INFINITY : tm[g] - m[g]);
+      if constexpr (WG == 2) {
+        if (key == 0) sPart[(t & 1) * 2 + wg] = cval;
+        named_bar_sync(1, kSoftmaxThreads);
+        cval = fmaxf(sPart[(t & 1) * 2], sPart[(t & 1) * 2 + 1]);
+      }
       const bool skip = kVote && cval < thr_raw;
       if (tid == 0) {
         const long gi = static_cast<long>(bk) * row_stride + j0 + t;
@@ -428,9 +447,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       }
       if (skip) continue;  // skipped tiles never raise m (lambda <= 1)
 
-      float mn[GP];
+      float mn[HG];
 #pragma unroll
-      for (int g = 0; g < GP; ++g) mn[g] = fmaxf(m[g], tm[g]);
+      for (int g = 0; g < HG; ++g) mn[g] = fmaxf(m[g], tm[g]);
       if (kPV) {
         const int sl = kept % NV;
         // The slot's previous tile (kept - NV) must be through its P.V MMA
@@ -445,17 +464,19 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           accumulate(kept - NV);
         }
         // P for this tile as the value MMA's B operand: NQ rows x 128 keys,
-        // K-major, 128-byte swizzle; this thread writes column `key`.
+        // K-major, 128-byte swizzle; this thread writes column `key` of its
+        // warpgroup's rows.
         uint8_t* ps = sP + sl * C::kPBytes + (key >> 6) * NQ * 128 + (key & 7) * 2;
         const int j8 = (key & 63) >> 3;
 #pragma unroll
-        for (int g = 0; g < GP; ++g) {
+        for (int g = 0; g < HG; ++g) {
           const float alpha = (m[g] == -INFINITY) ? 0.f : ex2_approx((m[g] - mn[g]) * sl2);
           const float mb = (mn[g] == -INFINITY) ? 0.f : mn[g] * sl2;
           const float pv = ex2_approx(fmaf(s[g], sl2, -mb));
           l[g] = fmaf(l[g], alpha, pv);
-          if (g < G)
-            *reinterpret_cast<__nv_bfloat16*>(ps + g * 128 + ((j8 ^ (g & 7)) << 4)) =
+          const int row = hg + g;
+          if (row < G)
+            *reinterpret_cast<__nv_bfloat16*>(ps + row * 128 + ((j8 ^ (row & 7)) << 4)) =
                 __float2bfloat16_rn(pv);
         }
         if (paged && tile_rows(t) < kTile) {
@@ -463,7 +484,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           // holds (TMA fills only rows outside the tensor map with zeros):
           // zero them so that P = 0 there cannot meet a non-finite V.
           ok = wwait(&ctl->v_full[sl], (kept / NV) & 1) && ok;
-          if (key >= tile_rows(t)) {
+          if (wg == 0 && key >= tile_rows(t)) {
 #pragma unroll
             for (int c = 0; c < C::kChunks; ++c) {
               uint4* row = reinterpret_cast<uint4*>(sV + sl * C::kTileBytes + c * 16384 + key * 128);
@@ -474,9 +495,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         }
         float mine_m = 0.f;
 #pragma unroll
-        for (int g = 0; g < GP; ++g)
-          if (tid == g) mine_m = mn[g];
-        if (tid < GP) sMs[(kept % (2 * NV)) * GP + tid] = mine_m;
+        for (int g = 0; g < HG; ++g)
+          if (key == g) mine_m = mn[g];
+        if (key < HG) sMs[(kept % (2 * NV)) * GP + hg + key] = mine_m;
         if (tid == 0) ctl->prec[sl] = 1;
         fence_proxy_async_smem();
         tc_fence_before();
@@ -485,7 +506,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         ++kept;
       }
 #pragma unroll
-      for (int g = 0; g < GP; ++g) m[g] = mn[g];
+      for (int g = 0; g < HG; ++g) m[g] = mn[g];
     }
 
     if (kPV) {
@@ -501,29 +522,29 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->p_full[sl]);
-      named_bar_sync(1, 128);  // the last tile's maxima (sMs) are visible
+      named_bar_sync(1, kSoftmaxThreads);  // the last tile's maxima (sMs) are visible
       for (int j = max(0, kept - NV); j < kept; ++j) {
         ok = wwait(&ctl->slot_free[j % NV], (j / NV) & 1) && ok;
         tc_fence_after();
         accumulate(j);
       }
-      // Row sums: per-key partials over the 128 threads.
+      // Row sums: per-key partials over the warpgroup's 128 threads.
 #pragma unroll
-      for (int g = 0; g < GP; ++g) {
+      for (int g = 0; g < HG; ++g) {
         float v = l[g];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) sLRed[g * 4 + warp] = v;
+        if (lane == 0) sLRed[(hg + g) * 4 + wq] = v;
       }
-      named_bar_sync(1, 128);
+      named_bar_sync(1, kSoftmaxThreads);
       if (ok && !*abort_flag && key < D) {
         const int e = key;
 #pragma unroll
-        for (int g = 0; g < GP; ++g) {
-          if (g >= G) break;
-          const float4 r = *reinterpret_cast<const float4*>(sLRed + g * 4);
+        for (int g = 0; g < HG; ++g) {
+          if (hg + g >= G) break;
+          const float4 r = *reinterpret_cast<const float4*>(sLRed + (hg + g) * 4);
           const float lt = (r.x + r.y) + (r.z + r.w);
-          const size_t row = static_cast<size_t>(b) * p.Hq + kvh * G + g;
+          const size_t row = static_cast<size_t>(b) * p.Hq + kvh * G + hg + g;
           if (p.S == 1) {
             p.o[row * D + e] = __float2bfloat16_rn(lt > 0.f ? acc[g] / lt : 0.f);
           } else {
@@ -549,7 +570,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   }
 
   // ------------------------------------------------------------------ teardown
-  barrier_sync(2, kDecThreads);
+  barrier_sync(2, kDecThreads<GP>);
   if (warp == kWarpS) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
@@ -597,7 +618,7 @@ cudaError_t launch_dec(const CUtensorMap& tk, const CUtensorMap& tv, const Decod
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const long ctas = static_cast<long>(p.B) * p.Hkv * p.S;
-  fn<<<dim3(static_cast<unsigned>(ctas)), dim3(kDecThreads), C::kSmemBytes, st>>>(tk, tv, p);
+  fn<<<dim3(static_cast<unsigned>(ctas)), dim3(kDecThreads<GP>), C::kSmemBytes, st>>>(tk, tv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess || MODE == Mode::kCount || p.S == 1) return e;
   const int rows = p.B * p.Hq;
