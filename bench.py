@@ -365,20 +365,25 @@ def run_native(args):
         dist.destroy_process_group()
 
 
-def _time_ms(fn, iters=10, warmup=3):
+def _time_ms(fn, iters=6, warmup=3, batches=5):
+    """Median over `batches` of the mean device time of `iters` back-to-back
+    calls (CUDA events on the current stream).  Back to back, the host's
+    per-call work (argument checks, marshalling, launch) overlaps the previous
+    call's kernels instead of leaving the GPU idle between two events."""
     import torch
 
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
     ts = []
-    for _ in range(iters):
+    for _ in range(batches):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        fn()
+        for _ in range(iters):
+            fn()
         e1.record()
         e1.synchronize()
-        ts.append(e0.elapsed_time(e1))
+        ts.append(e0.elapsed_time(e1) / iters)
     ts.sort()
     return ts[len(ts) // 2]
 
