@@ -27,6 +27,21 @@ MUTATIONS = {
                                     "* p->Lk * dk;\n    const uint16_t* vh = v + (size_t)(b * p->Hkv + kvh) * p->Lk * dk;"),
     "value_row_stride_key_width": ("vh + (size_t)(k0 + t) * d;", "vh + (size_t)(k0 + t) * dk;"),
     "v_transposed": ("p * bf16_to_double(vk[e])", "p * bf16_to_double(vh[(size_t)e * d + (k0 + t) % d])"),
+    "O_not_rescaled": ("for (int e = 0; e < d; ++e) Or[e] *= alpha;", ""),
+    "tie_skips": ("(c < ln_lambda)", "(c <= ln_lambda)"),
+    "masked_row_vetoes": ("if (tmax[r] == -INFINITY) continue; /* no visible key: no veto */", ""),
+    "not_evaluated_counted_as_skipped": ("*c_out = NAN;\n    return ORC_NOT_EVALUATED;",
+                                         "*c_out = NAN;\n    return ORC_SKIPPED;"),
+    "causal_diagonal_excluded": ("row + off : (int64_t)p->Lk - 1", "row + off - 1 : (int64_t)p->Lk - 1"),
+    "calib_floor_not_round": ("floor(target * (double)N + 0.5)", "floor(target * (double)N)"),
+    "calib_unreachable_gives_zero": ("      a = L;\n", "      a = 0.0;\n"),
+    "causal_mask_ignored": ("if (key <= last_visible[r]) x = scale", "x = scale"),
+    "margin_after_update": ("const double diff = (st->m[r] == -INFINITY) ? INFINITY : tmax[r] - st->m[r];",
+                            "const double diff = (st->m[r] == -INFINITY) ? INFINITY : "
+                            "tmax[r] - (tmax[r] > st->m[r] ? tmax[r] : st->m[r]);"),
+    "split_state_carried_over": ("      /* Each split runs its own online pass from an empty state. */\n"
+                                 "      state_reset(&st);", "      if (sp == 0) state_reset(&st);"),
+    "merge_l_unweighted": ("l += ls * w;", "l += ls;"),
 }
 
 

@@ -474,6 +474,22 @@ def test_calibration_skips_exactly_round_sN(oracle_lib, target):
         assert c[want - 1] < math.log(lam) < c[want]
 
 
+def test_calibration_rounds_half_up(oracle_lib):
+    """k = round(s N), not floor(s N): a target whose s N has a fractional
+    part of 3/4 (inside the reachable range) skips one tile more than the
+    floor would."""
+    shape = (1, 4, 2, 64, 64, 8, True, 8, 4)
+    Lk = shape[4]
+    _, res0 = run_prefill_case(oracle_lib, shape, 0.0, 8, hot=True)
+    c = np.sort(res0.margin[res0.mask != 2])
+    N, reach = c.size, int((c < 0).sum())
+    k0 = reach // 2
+    assert 1 <= k0 < reach - 1
+    a, skipped, n_eval = oracle_lib.calibrate(res0.margin, res0.mask, (k0 + 0.75) / N, Lk)
+    assert n_eval == N and skipped == k0 + 1
+    assert c[k0] < math.log(a / Lk) < c[k0 + 1]
+
+
 def test_synthetic_hot_tiles_are_the_kept_set(oracle_lib):
     """Tiny prefill workload: only the hot tiles survive at a in {1, 4}.
 
@@ -494,3 +510,55 @@ def test_synthetic_hot_tiles_are_the_kept_set(oracle_lib):
         assert res.counts.sum() == 8 * (nT - 2)
         fin = np.isfinite(res.margin)
         assert (np.abs(res.margin[fin] - math.log(a / 1024)) > 2.0).all()
+
+
+# ------------------------------------------------- readings at the boundary
+def test_tie_keeps_the_tile(oracle_lib):
+    """The comparison is strict: a tile whose maximum equals the running
+    maximum has c_j = 0 exactly, and lambda = 1 (ln lambda = 0) keeps it.
+
+    Tile 1 is a bit-for-bit copy of tile 0, so every row's tile maximum
+    repeats its running maximum."""
+    rng = np.random.default_rng(5)
+    d, Bq, Bk = 4, 4, 4
+    q = rand_bits(rng, (1, 1, 4, d))
+    k0 = rand_bits(rng, (1, 1, 4, d))
+    v = rand_bits(rng, (1, 1, 8, d))
+    k = np.concatenate([k0, k0], axis=2)
+    res = oracle_lib.prefill(q, k, v, scale=0.5, causal=False, lam=1.0, Bq=Bq, Bk=Bk)
+    assert res.margin[0, 1] == 0.0
+    assert res.mask[0].tolist() == [0, 0] and int(res.counts[0]) == 0
+    ref = two_pass(f64(q[0, 0]), f64(k[0, 0]), f64(v[0, 0]), 0.5, visible(4, 8, False))
+    np.testing.assert_allclose(res.o[0, :4], ref, rtol=0, atol=1e-12)
+    # just below lambda = 1 the same tile is still kept (c_j = 0 > ln lambda is false)
+    res2 = oracle_lib.prefill(q, k, v, scale=0.5, causal=False, lam=np.nextafter(1.0, 0.0),
+                              Bq=Bq, Bk=Bk)
+    assert res2.mask[0].tolist() == [0, 0]
+
+
+def test_row_without_any_key_does_not_veto(oracle_lib):
+    """Causal with Lq > Lk (bottom-right): rows 0-2 of the first block see no
+    key at all; the other rows' votes alone decide each tile.
+
+    Lq = 11, Lk = 8, Bq = 8, Bk = 2, offset Lk - Lq = -3: row r sees keys
+    <= r - 3.  Every query is e1; keys 0-1 are 8 e1 (score 4 at scale 1/2),
+    keys 2-7 are -8 e1 (score -4), so every later tile has c_j = -8 for the
+    rows that see it.  At lambda = 0.01 (ln = -4.6) those tiles are skipped;
+    tile 3 (keys 6, 7) is seen by no row of block 0: not evaluated."""
+    d = 4
+    q = np.zeros((1, 1, 11, d), np.float32)
+    q[..., 0] = 1.0
+    kx = np.zeros((1, 1, 8, d), np.float32)
+    kx[..., :2, 0] = 8.0
+    kx[..., 2:, 0] = -8.0
+    rng = np.random.default_rng(6)
+    v = rand_bits(rng, (1, 1, 8, d))
+    res = oracle_lib.prefill(bf16_bits(q), bf16_bits(kx), v, scale=0.5, causal=True, lam=0.01,
+                             Bq=8, Bk=2)
+    assert res.mask[0].tolist() == [0, 1, 1, 2] and int(res.counts[0]) == 2
+    assert res.mask[1].tolist() == [0, 1, 1, 1] and int(res.counts[1]) == 3
+    np.testing.assert_allclose(res.margin[0, 1:3], [-8.0, -8.0], rtol=0, atol=1e-12)
+    assert not res.o[0, :3].any()  # rows with no visible key return zeros
+    # rows that kept only tile 0 average its two values (equal scores)
+    vk = f64(v[0, 0])
+    np.testing.assert_allclose(res.o[0, 4], 0.5 * (vk[0] + vk[1]), rtol=0, atol=1e-12)
