@@ -42,6 +42,10 @@ MUTATIONS = {
     "split_state_carried_over": ("      /* Each split runs its own online pass from an empty state. */\n"
                                  "      state_reset(&st);", "      if (sp == 0) state_reset(&st);"),
     "merge_l_unweighted": ("l += ls * w;", "l += ls;"),
+    "split_size_floor_plus_one": ("T = ceil_div(nT, S)", "T = nT / S + 1"),
+    "decode_heads_interleaved": ("q + ((size_t)b * p->Hq + (size_t)kvh * G + g) * dk;",
+                                 "q + ((size_t)b * p->Hq + (size_t)g * p->Hkv + kvh) * dk;"),
+    "calib_lambda_above_one": ("if (hi > 0.0) hi = 0.0; /* lambda <= 1 */", ""),
 }
 
 

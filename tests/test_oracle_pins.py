@@ -290,6 +290,8 @@ DECODE_SHAPES = [
     (1, 4, 4, 50, 6, 4, 5),
     (3, 4, 1, 9, 4, 8, 4),     # more splits than tiles: empty splits
     (1, 2, 1, 300, 64, 2, 128),
+    (2, 4, 2, 64, 8, 4, 4),     # splits that divide the 16 tiles: 4 tiles each
+    (1, 8, 1, 48, 8, 2, 4),     # 12 tiles in 2 splits of 6
 ]
 
 
