@@ -92,23 +92,32 @@ class ClockSampler:
         self.proc.terminate()
         self.proc.wait(timeout=10)
         self.f.close()
-        rows = []
-        for line in open(self.path):
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
-            except ValueError:
-                continue
+        with open(self.path) as f:
+            lines = f.readlines()
         os.unlink(self.path)
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for _, _, r in rows for i in range(4) if r[i] == "Active"})
-        loaded = [r[0] for r in rows if r[0] > 0.5 * r[1]] or [r[0] for r in rows]
-        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(rows)}
+        return parse_clock_samples(lines)
+
+
+def parse_clock_samples(lines):
+    """Summarise nvidia-smi samples (csv, noheader, nounits, in ClockSampler.FIELDS
+    order): median SM clock over the samples above half the maximum (under
+    load), the maximum, and every throttle reason seen active."""
+    rows = []
+    for line in lines:
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 9:
+            continue
+        try:
+            rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+        except ValueError:
+            continue
+    if not rows:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    reasons = sorted({names[i] for _, _, r in rows for i in range(4) if r[i] == "Active"})
+    loaded = [r[0] for r in rows if r[0] > 0.5 * r[1]] or [r[0] for r in rows]
+    return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(r[1] for r in rows),
+            "reasons": reasons, "samples": len(rows)}
 
 
 def _dist():

@@ -75,3 +75,26 @@ def test_reference_arm_other_ranks_exit_quietly():
                        timeout=300, cwd=ROOT)
     assert r.returncode == 0, r.stderr[-2000:]
     assert r.stdout.strip() == ""
+
+
+def test_clock_samples_summary():
+    """The clocks record of the bench line: median SM clock under load, the
+    maximum, and the throttle reasons seen active (what decides whether a
+    number is kept)."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    na = "Not Active"
+    lines = [
+        f"0, 2070, 2070, 900.1, 0x0, {na}, {na}, {na}, {na}\n",
+        f"0, 1980, 2070, 1390.0, 0x4, {na}, {na}, {na}, Active\n",
+        f"0, 2010, 2070, 1385.2, 0x4, {na}, {na}, {na}, Active\n",
+        f"0, 345, 2070, 120.0, 0x1, {na}, {na}, {na}, {na}\n",  # idle sample: not under load
+        "garbled line\n",
+    ]
+    got = bench.parse_clock_samples(lines)
+    assert got["sm_mhz"] == 2010 and got["sm_max_mhz"] == 2070 and got["samples"] == 4
+    assert got["reasons"] == ["sw_power_cap"]
+    hot = bench.parse_clock_samples([f"0, 1500, 2070, 1400, 0x40, Active, {na}, Active, {na}\n"])
+    assert hot["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
+    assert bench.parse_clock_samples([])["reasons"] == ["no samples"]
