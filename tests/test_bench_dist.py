@@ -98,3 +98,24 @@ def test_clock_samples_summary():
     hot = bench.parse_clock_samples([f"0, 1500, 2070, 1400, 0x40, Active, {na}, Active, {na}\n"])
     assert hot["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
     assert bench.parse_clock_samples([])["reasons"] == ["no samples"]
+
+
+def test_clock_sampler_with_a_fake_nvidia_smi(tmp_path, monkeypatch):
+    """ClockSampler start/stop end to end, with a stand-in nvidia-smi on PATH
+    that prints two samples and then waits to be terminated."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    fake = tmp_path / "nvidia-smi"
+    fake.write_text("#!/bin/sh\n"
+                    "echo '0, 2055, 2070, 1200.5, 0x4, Not Active, Not Active, Not Active, Active'\n"
+                    "echo '0, 2070, 2070, 1100.0, 0x0, Not Active, Not Active, Not Active, Not Active'\n"
+                    "exec sleep 30\n")
+    fake.chmod(0o755)
+    monkeypatch.setenv("PATH", f"{tmp_path}{os.pathsep}{os.environ['PATH']}")
+    cs = bench.ClockSampler(0)
+    cs.start()
+    got = cs.stop()
+    assert got == {"sm_mhz": 2062.5, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"],
+                   "samples": 2}
+    assert not os.path.exists(cs.path)
