@@ -119,3 +119,26 @@ def test_clock_sampler_with_a_fake_nvidia_smi(tmp_path, monkeypatch):
     assert got == {"sm_mhz": 2062.5, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"],
                    "samples": 2}
     assert not os.path.exists(cs.path)
+
+
+def test_reference_arm_line_on_the_host():
+    """The reference arm (the oracle on host cores) prints one JSON line with
+    the native arm's metric and unit, its core count and zero-byte e2e."""
+    import json
+
+    env = dict(os.environ, OMP_NUM_THREADS="2")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "0"], env=env, capture_output=True, text=True,
+                       timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    sys.path.insert(0, ROOT)
+    import bench
+
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "TFLOP/s"
+    assert d["value"] > 0 and d["higher_is_better"] is True and d["warmup"] >= 3
+    assert d["cpu_baseline"]["cores"] == 2 and d["cpu_baseline"]["kind"] == "oracle"
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["e2e"]["value"] == d["value"]
