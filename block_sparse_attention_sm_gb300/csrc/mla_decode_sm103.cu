@@ -1,8 +1,9 @@
 // Skip-softmax (BLASST) split-KV decode for multi-head latent attention
 // (MLA) on sm_103a, plus the log-sum-exp merge of the splits.
 //
-// The "Skip-Softmax" design doc lists MLA among the attention kinds the skip
-// test applies to, without shapes.  Read here in the absorbed decode form:
+// The BLASST summary lists MLA among the attention kinds its prefill and
+// decode kernels support (§Belangrijkste Bijdragen, item 4: MHA, GQA, MQA and
+// MLA), without shapes.  Read here in the absorbed decode form:
 // every sequence keeps one latent cache row per token, 512 latent entries
 // followed by 64 rotary entries; the keys are the whole 576-entry rows, the
 // values their 512 latent entries, and all Hq query heads share that one

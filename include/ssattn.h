@@ -218,15 +218,17 @@ ss_status ss_attn_decode_noalloc(const void* q, const void* k_cache, const void*
 
 /*
  * Latent-attention (MLA) decode: the skip test on multi-head latent
- * attention, which the "Skip-Softmax" design doc lists among the supported
- * attention kinds without giving its shapes.  Read as the absorbed decode
+ * attention, which the BLASST summary names among the attention kinds its
+ * prefill and decode kernels support (§Belangrijkste Bijdragen, item 4:
+ * MHA, GQA, MQA and MLA), without giving its shapes.  Read as the absorbed decode
  * form: each sequence caches one latent row per token, d_latent latent
  * entries followed by d_rope rotary entries; the keys are the whole rows
  * (width dk = d_latent + d_rope), the values their first d_latent entries,
  * and every query head attends to that one latent head.  All Hq heads of a
  * sequence are therefore the voting group of a tile: a tile is skipped only
  * if exp(tile_max - running_max) < lambda holds for every head (BLASST
- * summary, §Methodologie; "Skip-Softmax" §What this bounds).  The split of
+ * summary, §Methodologie; "Skip-Softmax" §What this bounds: one decision
+ * per tile).  The split of
  * the nT = ceil(Lk/128) tiles into num_kv_splits contiguous ranges and the
  * log-sum-exp merge are those of ss_attn_decode.  The values are read from
  * the key rows already on chip, so a skipped tile saves the exponentials and

@@ -184,8 +184,10 @@ def mla_decode(q, kv, *, d_latent: int, scale: float, lam: float, num_splits: in
     """Decode with multi-head latent attention over q [B,Hq,dk] and one
     latent cache kv [B,Lk,dk] (bf16) shared by every query head.
 
-    Reading of the pages' "MLA" (the "Skip-Softmax" design doc lists it among
-    the supported attention kinds without giving its shapes): the absorbed
+    Reading of the pages' "MLA" (the BLASST summary, §Belangrijkste
+    Bijdragen item 4, lists it beside MHA, GQA and MQA among the attention
+    kinds its prefill and decode kernels support, without giving its
+    shapes): the absorbed
     form, in which the keys are the cache rows (latent part followed by the
     rotary part, dk wide) and the values are their first d_latent entries.
     All Hq heads share the one latent head, so they form the voting group.

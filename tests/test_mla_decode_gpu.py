@@ -2,8 +2,9 @@
 
 The keys are the 576-entry latent cache rows (512 latent + 64 rotary
 entries), the values their latent part, and all query heads of a sequence
-vote together on each tile ("Skip-Softmax" design doc: MLA listed among the
-supported attention kinds; the absorbed-form reading is the oracle's).
+vote together on each tile (BLASST summary, §Belangrijkste Bijdragen item 4:
+MLA listed beside MHA, GQA and MQA among the attention kinds the kernels
+support; the absorbed-form reading is the oracle's).
 """
 import numpy as np
 import pytest
