@@ -19,7 +19,8 @@ SS_PREFILL, SS_DECODE, SS_MLA_DECODE = 0, 1, 2
 
 EXPORTS = (
     "ss_attn_prefill", "ss_attn_prefill_ex", "ss_attn_decode_workspace_size", "ss_attn_decode",
-    "ss_attn_decode_ex", "ss_attn_decode_noalloc", "ss_attn_decode_paged",
+    "ss_attn_decode_ex", "ss_attn_decode_noalloc", "ss_decode_static_scratch_bytes",
+    "ss_attn_decode_paged",
     "ss_attn_mla_decode_workspace_size", "ss_attn_mla_decode", "ss_attn_mla_decode_ex",
     "ss_attn_mla_decode_paged",
     "ss_calibrate", "ss_fit_factor", "ss_lambda", "ss_status_string", "ss_stream_status",
@@ -44,7 +45,7 @@ class ss_problem(ctypes.Structure):
                 ("Hkv", ctypes.c_int), ("Lq", ctypes.c_int), ("Lk", ctypes.c_int),
                 ("d", ctypes.c_int), ("scale", ctypes.c_float), ("causal", ctypes.c_int),
                 ("num_kv_splits", ctypes.c_int), ("skip_counts", ctypes.c_void_p),
-                ("stream", ctypes.c_void_p)]
+                ("stream", ctypes.c_void_p), ("fault_inject", ctypes.c_int)]
 
 
 _lib = None
@@ -67,6 +68,8 @@ def load() -> ctypes.CDLL:
     lib.ss_attn_decode.argtypes = dec + [P]
     lib.ss_attn_decode_ex.argtypes = dec + [ctypes.POINTER(ss_debug_opts), P]
     lib.ss_attn_decode_noalloc.argtypes = [P, P, P, P, I, I, I, I, I, F, F, I, P, P]
+    lib.ss_decode_static_scratch_bytes.argtypes = []
+    lib.ss_decode_static_scratch_bytes.restype = U
     lib.ss_attn_decode_paged.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, F, F, I, P, P, U,
                                          ctypes.POINTER(ss_debug_opts), P]
     lib.ss_attn_decode_workspace_size.argtypes = [I, I, I, I]
@@ -181,7 +184,12 @@ def ss_attn_decode_paged(q, k_pages, v_pages, page_table, seq_lens, o, B, Hq, Hk
                                        ctypes.byref(dbg), _stream(stream))
 
 
-SS_DECODE_STATIC_SCRATCH_BYTES = 16 << 20
+SS_DECODE_STATIC_SCRATCH_BYTES = 16 << 20  # the header's value; test_abi checks the library's
+
+
+def ss_decode_static_scratch_bytes() -> int:
+    """Size of ss_attn_decode_noalloc's built-in array in the loaded library."""
+    return int(load().ss_decode_static_scratch_bytes())
 
 
 def ss_attn_mla_decode_workspace_size(B, Hq, d_latent, num_kv_splits) -> int:

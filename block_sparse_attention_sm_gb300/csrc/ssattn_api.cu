@@ -519,6 +519,8 @@ ss_status ss_attn_decode_noalloc(const void* q, const void* k_cache, const void*
                      skip_counts, ws, SS_DECODE_STATIC_SCRATCH_BYTES, nullptr, stream);
 }
 
+size_t ss_decode_static_scratch_bytes(void) { return SS_DECODE_STATIC_SCRATCH_BYTES; }
+
 ss_status ss_calibrate(const ss_problem* p, float target_sparsity, float* a_out,
                        float* achieved_out) {
   if (p == nullptr || a_out == nullptr || p->skip_counts == nullptr || !aligned16(p->q) ||
@@ -536,6 +538,7 @@ ss_status ss_calibrate(const ss_problem* p, float target_sparsity, float* a_out,
   std::vector<uint32_t> host(ncnt);
   ss_debug_opts dbg{};
   dbg.count_only = 1;
+  dbg.fault_inject = (p->kind == SS_DECODE) ? p->fault_inject : 0;
 
   // Skipped tiles at lambda = exp(ln_lambda), from one count-only launch.
   auto count_at = [&](double ln_lambda, long* out) -> ss_status {
@@ -555,6 +558,16 @@ ss_status ss_calibrate(const ss_problem* p, float target_sparsity, float* a_out,
                         cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
         cudaStreamSynchronize(stream) != cudaSuccess)
       return SS_ERR_CUDA;
+    // Counters of a launch that gave up a bounded wait are not trustworthy:
+    // read (and clear) the device status word before using them.
+    uint32_t dev_status = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&dev_status, g_device_status, sizeof dev_status) != cudaSuccess)
+      return SS_ERR_CUDA;
+    if (dev_status != 0) {
+      if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof zero) != cudaSuccess)
+        return SS_ERR_CUDA;
+      if (dev_status & kDevStatusTimeout) return SS_ERR_TIMEOUT;
+    }
     long s = 0;
     for (uint32_t c : host) s += c;
     *out = s;

@@ -211,6 +211,9 @@ ss_status ss_attn_decode_paged(const void* q, const void* k_pages, const void* v
  * race on the array: serialise them.
  */
 #define SS_DECODE_STATIC_SCRATCH_BYTES (16u << 20)
+/* The size of that array in the library as built (SS_DECODE_STATIC_SCRATCH_BYTES
+   of the header it was compiled with); host only, needs no GPU. */
+size_t ss_decode_static_scratch_bytes(void);
 ss_status ss_attn_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
                                  void* o, int B, int Hq, int Hkv, int Lk, int d, float scale,
                                  float lambda, int num_kv_splits, uint32_t* skip_counts,
@@ -312,6 +315,10 @@ typedef struct {
      latent decode: B*num_kv_splits). */
   uint32_t* skip_counts;
   void* stream;
+  /* Test only, SS_DECODE only (0 otherwise): passed to every count-only
+     launch as ss_debug_opts.fault_inject, so that a bounded wait expires and
+     the calibration's handling of it can be tested. */
+  int fault_inject;
 } ss_problem;
 
 /*
@@ -322,7 +329,10 @@ typedef struct {
  * tile counters back after each, and returns the log-midpoint of the
  * interval of a that hits the target count (the widest margin), clamped to
  * lambda <= 1.  When the target is not reachable under lambda <= 1 it
- * returns the a closest to it.  Synchronises p->stream.
+ * returns the a closest to it.  Synchronises p->stream.  After each count-only
+ * launch it reads and clears the device status word (that of
+ * ss_stream_status): if a kernel gave up a bounded wait, the counters are not
+ * used and the call returns SS_ERR_TIMEOUT.
  *   a_out: the fitted a (0 when the target rounds to zero skipped tiles).
  *   achieved_out (nullable): skipped / evaluated at the returned a.
  */

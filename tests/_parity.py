@@ -9,10 +9,23 @@ Acceptance (per unit):
 * outputs agree within max-abs 2e-2 and mean-abs 2e-3 (bf16 output), both
   against the oracle with its own decisions (units without disagreement) and
   against the oracle re-run under the GPU's decisions (arithmetic only).
+
+Every check returns a `Parity` record (units, evaluated tiles, near-margin
+tiles, disagreements, errors) and appends it to `LOG`; conftest.py prints the
+session's records and totals at the end of the run, so the near-margin
+disagreements are reported, not only tolerated.
+
+Every output the kernels write (o, counters, skip mask, vote margins) sits in
+a buffer with a guard band of GUARD_BYTES on each side, filled with the byte
+GUARD_BYTE; after each call the bands must be intact.  This is the bounds
+check of the outputs (a store one element past the end, or before the start,
+of any output fails the test).
 """
 from __future__ import annotations
 
+import dataclasses
 import math
+import os
 
 import numpy as np
 import torch
@@ -24,6 +37,71 @@ MAX_ABS = 2e-2
 MEAN_ABS = 2e-3
 NEAR_MARGIN = 1e-2
 TILE = 128
+GUARD_BYTES = 256  # keeps the guarded view 256-byte aligned
+GUARD_BYTE = 0xA5
+
+
+@dataclasses.dataclass
+class Parity:
+    """Outcome of one parity check (one launch, the sampled units of it)."""
+    kind: str
+    lam: float
+    units: int = 0
+    tiles: int = 0          # evaluated (unit, tile) pairs compared
+    skipped: int = 0        # tiles the GPU skipped among them
+    near: int = 0           # of which the oracle's |c_j - ln lambda| < NEAR_MARGIN
+    disagree: int = 0       # decisions that differ (all of them near-margin)
+    max_abs: float = 0.0    # output error against the oracle's own decisions
+    mean_abs: float = 0.0
+    max_abs_gpu_mask: float = 0.0  # against the oracle run under the GPU's decisions
+    test: str = ""
+
+    def add_decisions(self, gmask, omask, omargin, lam):
+        ev = omask != 2
+        self.tiles += int(ev.sum())
+        self.skipped += int((gmask == 1).sum())
+        self.near += int((ev & (np.abs(omargin - _ln(lam)) < NEAR_MARGIN)).sum())
+
+    def add_error(self, err, own_mask: bool):
+        if own_mask:
+            self.max_abs = max(self.max_abs, err[0])
+            # mean over units, weighted equally (each unit's mean is bounded)
+            self.mean_abs = max(self.mean_abs, err[1])
+        else:
+            self.max_abs_gpu_mask = max(self.max_abs_gpu_mask, err[0])
+
+
+LOG: list[Parity] = []
+
+
+def _finish(rec: Parity) -> Parity:
+    rec.test = os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0]
+    LOG.append(rec)
+    return rec
+
+
+class Guarded:
+    """A device tensor of `shape` inside a buffer with guard bands."""
+
+    def __init__(self, shape, dtype, device, fill):
+        self.n = int(np.prod(shape)) if len(shape) else 1
+        item = torch.empty((), dtype=dtype).element_size()
+        self.g = GUARD_BYTES // item
+        self.buf = torch.empty(self.n + 2 * self.g, dtype=dtype, device=device)
+        self.buf.view(torch.uint8).fill_(GUARD_BYTE)
+        self.t = self.buf[self.g:self.g + self.n].view(shape)
+        self.t.fill_(fill)
+
+    def check(self, what):
+        raw = self.buf.view(torch.uint8)
+        nb = self.g * self.buf.element_size()
+        head, tail = raw[:nb], raw[raw.numel() - nb:]
+        assert bool((head == GUARD_BYTE).all()), f"{what}: write before the start of the output"
+        assert bool((tail == GUARD_BYTE).all()), f"{what}: write past the end of the output"
+
+
+def guarded(shape, dtype, device, fill):
+    return Guarded(tuple(shape), dtype, device, fill)
 
 
 def _ln(lam):
@@ -72,23 +150,28 @@ def gpu_prefill_all(q, k, v, scale, causal, lam, chunk=0):
     nqb, nT = -(-Lq // TILE), -(-Lk // TILE)
     n_units = B * Hq * nqb
     dev = q.device
-    o = torch.empty_like(q)
-    counts = torch.full((n_units,), -1, dtype=torch.int32, device=dev)
+    og = guarded(q.shape, q.dtype, dev, float("nan"))
+    cg = guarded((n_units,), torch.int32, dev, -1)
+    o, counts = og.t, cg.t
     if chunk == 0:
         st = capi.ss_attn_prefill(q, k, v, o, B, Hq, Hkv, Lq, Lk, d, scale, causal, lam, counts)
     else:
         st = capi.ss_attn_prefill_ex(q, k, v, o, B, Hq, Hkv, Lq, Lk, d, scale, causal, lam,
                                      counts, vote_chunk_tiles=chunk)
     assert st == capi.SS_OK, capi.ss_status_string(st)
-    o2 = torch.empty_like(q)
-    counts2 = torch.full((n_units,), -1, dtype=torch.int32, device=dev)
-    mask = torch.full((n_units, nT), 7, dtype=torch.uint8, device=dev)
-    margin = torch.full((n_units, nT), 12345.0, dtype=torch.float32, device=dev)
+    o2g = guarded(q.shape, q.dtype, dev, float("nan"))
+    c2g = guarded((n_units,), torch.int32, dev, -1)
+    mg = guarded((n_units, nT), torch.uint8, dev, 7)
+    gg = guarded((n_units, nT), torch.float32, dev, 12345.0)
+    o2, counts2, mask, margin = o2g.t, c2g.t, mg.t, gg.t
     st = capi.ss_attn_prefill_ex(q, k, v, o2, B, Hq, Hkv, Lq, Lk, d, scale, causal, lam, counts2,
                                  mask, margin, vote_chunk_tiles=chunk)
     assert st == capi.SS_OK, capi.ss_status_string(st)
     assert capi.ss_stream_status() == capi.SS_OK
     torch.cuda.synchronize()
+    for gb, what in ((og, "o"), (cg, "skip_counts"), (o2g, "o (debug call)"),
+                     (c2g, "skip_counts (debug call)"), (mg, "skip_mask"), (gg, "vote_margin")):
+        gb.check(what)
     # The debug outputs do not change the result.  (lambda = 0 with debug
     # outputs runs the voting kernel with nothing skipped instead of the
     # dense kernel: the same values up to rounding.)
@@ -101,10 +184,8 @@ def gpu_prefill_all(q, k, v, scale, causal, lam, chunk=0):
     return o, counts, mask, margin
 
 
-def check_prefill(q, k, v, *, scale, causal, lam, units=None, chunk=0):
-    """Parity of one prefill launch; `units` = list of (b, h, qb) or None (all).
-
-    Returns the number of near-margin disagreements."""
+def check_prefill(q, k, v, *, scale, causal, lam, units=None, chunk=0) -> Parity:
+    """Parity of one prefill launch; `units` = list of (b, h, qb) or None (all)."""
     B, Hq, Lq, d = q.shape
     _, Hkv, Lk, _ = k.shape
     G = Hq // Hkv
@@ -115,7 +196,7 @@ def check_prefill(q, k, v, *, scale, causal, lam, units=None, chunk=0):
     by_head = {}
     for (b, h, qb) in units:
         by_head.setdefault((b, h), []).append(qb)
-    n_dis = 0
+    rec = Parity("prefill", lam)
     counts_h = counts.cpu().numpy()
     mask_h = mask.cpu().numpy()
     margin_h = margin.cpu().numpy()
@@ -126,7 +207,9 @@ def check_prefill(q, k, v, *, scale, causal, lam, units=None, chunk=0):
         gids = [(b * Hq + h) * nqb + qb for qb in qbs]
         gmask, gmargin = mask_h[gids], margin_h[gids]
         nd, row_dis = compare_decisions(gmask, gmargin, ref.mask, ref.margin, lam)
-        n_dis += nd
+        rec.units += len(qbs)
+        rec.disagree += nd
+        rec.add_decisions(gmask, ref.mask, ref.margin, lam)
         np.testing.assert_array_equal(counts_h[gids], (gmask == 1).sum(axis=1))
         for i, qb in enumerate(qbs):
             if not row_dis[i]:
@@ -136,13 +219,15 @@ def check_prefill(q, k, v, *, scale, causal, lam, units=None, chunk=0):
         og = o[b, h].float().cpu().numpy()
         for i, qb in enumerate(qbs):
             r0, r1 = qb * TILE, min(Lq, qb * TILE + TILE)
-            check_output(og[r0:r1], over.o[i, : r1 - r0], f"unit {(b, h, qb)} under GPU mask")
+            rec.add_error(check_output(og[r0:r1], over.o[i, : r1 - r0],
+                                       f"unit {(b, h, qb)} under GPU mask"), False)
             if not row_dis[i]:
-                check_output(og[r0:r1], ref.o[i, : r1 - r0], f"unit {(b, h, qb)}")
-    return n_dis
+                rec.add_error(check_output(og[r0:r1], ref.o[i, : r1 - r0], f"unit {(b, h, qb)}"),
+                              True)
+    return _finish(rec)
 
 
-def check_decode(q, k, v, *, scale, lam, num_splits, units=None):
+def check_decode(q, k, v, *, scale, lam, num_splits, units=None) -> Parity:
     """Parity of one decode launch; `units` = list of b*Hkv + kvh (None: all)."""
     B, Hq, d = q.shape
     _, Hkv, Lk, _ = k.shape
@@ -152,19 +237,24 @@ def check_decode(q, k, v, *, scale, lam, num_splits, units=None):
     dev = q.device
     ws_n = capi.ss_attn_decode_workspace_size(B, Hq, d, S)
     ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=dev)
-    o = torch.empty_like(q)
-    counts = torch.full((B * Hkv * S,), -1, dtype=torch.int32, device=dev)
+    og = guarded(q.shape, q.dtype, dev, float("nan"))
+    cg = guarded((B * Hkv * S,), torch.int32, dev, -1)
+    o, counts = og.t, cg.t
     st = capi.ss_attn_decode(q, k, v, o, B, Hq, Hkv, Lk, d, scale, lam, S, counts, ws, ws_n)
     assert st == capi.SS_OK, capi.ss_status_string(st)
-    o2 = torch.empty_like(q)
-    counts2 = torch.full_like(counts, -1)
-    mask = torch.full((B * Hkv, nT), 7, dtype=torch.uint8, device=dev)
-    margin = torch.full((B * Hkv, nT), 12345.0, dtype=torch.float32, device=dev)
+    o2g = guarded(q.shape, q.dtype, dev, float("nan"))
+    c2g = guarded((B * Hkv * S,), torch.int32, dev, -1)
+    mg = guarded((B * Hkv, nT), torch.uint8, dev, 7)
+    gg = guarded((B * Hkv, nT), torch.float32, dev, 12345.0)
+    o2, counts2, mask, margin = o2g.t, c2g.t, mg.t, gg.t
     st = capi.ss_attn_decode_ex(q, k, v, o2, B, Hq, Hkv, Lk, d, scale, lam, S, counts2, ws, ws_n,
                                 mask, margin)
     assert st == capi.SS_OK, capi.ss_status_string(st)
     assert capi.ss_stream_status() == capi.SS_OK
     torch.cuda.synchronize()
+    for gb, what in ((og, "o"), (cg, "skip_counts"), (o2g, "o (debug call)"),
+                     (c2g, "skip_counts (debug call)"), (mg, "skip_mask"), (gg, "vote_margin")):
+        gb.check(what)
     assert torch.equal(o, o2) and torch.equal(counts, counts2)
     if units is None:
         units = list(range(B * Hkv))
@@ -172,16 +262,18 @@ def check_decode(q, k, v, *, scale, lam, num_splits, units=None):
     ch = counts.cpu().numpy().reshape(B * Hkv, S)
     mh = mask.cpu().numpy()
     gh = margin.cpu().numpy()
-    og = o.float().cpu().numpy()
+    og_h = o.float().cpu().numpy()
     T = -(-nT // S)
-    n_dis = 0
+    rec = Parity("decode", lam)
     for u in units:
         b, kvh = divmod(u, Hkv)
         qs = q[b:b + 1, kvh * G:(kvh + 1) * G]
         ks, vs = k[b:b + 1, kvh:kvh + 1], v[b:b + 1, kvh:kvh + 1]
         ref = oracle.decode(qs, ks, vs, scale=scale, lam=lam, num_splits=S)
         nd, row_dis = compare_decisions(mh[u:u + 1], gh[u:u + 1], ref.mask, ref.margin, lam)
-        n_dis += nd
+        rec.units += 1
+        rec.disagree += nd
+        rec.add_decisions(mh[u:u + 1], ref.mask, ref.margin, lam)
         for sp in range(S):
             tiles = range(sp * T, min(nT, sp * T + T))
             gsk = int((mh[u, list(tiles)] == 1).sum()) if len(tiles) else 0
@@ -190,13 +282,15 @@ def check_decode(q, k, v, *, scale, lam, num_splits, units=None):
                 assert ch[u, sp] == ref.counts[0, sp]
         over = oracle.decode(qs, ks, vs, scale=scale, lam=lam, num_splits=S,
                              mask_override=(mh[u:u + 1] == 1).astype(np.uint8))
-        check_output(og[b, kvh * G:(kvh + 1) * G], over.o[0], f"decode unit {u} under GPU mask")
+        rec.add_error(check_output(og_h[b, kvh * G:(kvh + 1) * G], over.o[0],
+                                   f"decode unit {u} under GPU mask"), False)
         if not row_dis[0]:
-            check_output(og[b, kvh * G:(kvh + 1) * G], ref.o[0], f"decode unit {u}")
-    return n_dis
+            rec.add_error(check_output(og_h[b, kvh * G:(kvh + 1) * G], ref.o[0],
+                                       f"decode unit {u}"), True)
+    return _finish(rec)
 
 
-def check_mla(q, kv, *, scale, lam, num_splits, units=None, d_latent=512):
+def check_mla(q, kv, *, scale, lam, num_splits, units=None, d_latent=512) -> Parity:
     """Parity of one latent-attention decode launch; `units` = sequences."""
     B, Hq, dk = q.shape
     Lk = kv.shape[1]
@@ -205,20 +299,25 @@ def check_mla(q, kv, *, scale, lam, num_splits, units=None, d_latent=512):
     dev = q.device
     ws_n = capi.ss_attn_mla_decode_workspace_size(B, Hq, d_latent, S)
     ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=dev)
-    o = torch.full((B, Hq, d_latent), float("nan"), dtype=q.dtype, device=dev)
-    counts = torch.full((B * S,), -1, dtype=torch.int32, device=dev)
+    og = guarded((B, Hq, d_latent), q.dtype, dev, float("nan"))
+    cg = guarded((B * S,), torch.int32, dev, -1)
+    o, counts = og.t, cg.t
     st = capi.ss_attn_mla_decode(q, kv, o, B, Hq, Lk, d_latent, dk - d_latent, scale, lam, S,
                                  counts, ws, ws_n)
     assert st == capi.SS_OK, capi.ss_status_string(st)
-    o2 = torch.full_like(o, float("nan"))
-    counts2 = torch.full_like(counts, -1)
-    mask = torch.full((B, nT), 7, dtype=torch.uint8, device=dev)
-    margin = torch.full((B, nT), 12345.0, dtype=torch.float32, device=dev)
+    o2g = guarded((B, Hq, d_latent), q.dtype, dev, float("nan"))
+    c2g = guarded((B * S,), torch.int32, dev, -1)
+    mg = guarded((B, nT), torch.uint8, dev, 7)
+    gg = guarded((B, nT), torch.float32, dev, 12345.0)
+    o2, counts2, mask, margin = o2g.t, c2g.t, mg.t, gg.t
     st = capi.ss_attn_mla_decode_ex(q, kv, o2, B, Hq, Lk, d_latent, dk - d_latent, scale, lam, S,
                                     counts2, ws, ws_n, mask, margin)
     assert st == capi.SS_OK, capi.ss_status_string(st)
     assert capi.ss_stream_status() == capi.SS_OK
     torch.cuda.synchronize()
+    for gb, what in ((og, "o"), (cg, "skip_counts"), (o2g, "o (debug call)"),
+                     (c2g, "skip_counts (debug call)"), (mg, "skip_mask"), (gg, "vote_margin")):
+        gb.check(what)
     if lam > 0:
         assert torch.equal(o, o2) and torch.equal(counts, counts2)
     else:  # the plain call runs the dense kernel, the debug call the voting one
@@ -227,14 +326,16 @@ def check_mla(q, kv, *, scale, lam, num_splits, units=None, d_latent=512):
     units = sorted(range(B) if units is None else units)
     ch = counts.cpu().numpy().reshape(B, S)
     mh, gh = mask.cpu().numpy(), margin.cpu().numpy()
-    og = o.float().cpu().numpy()
+    og_h = o.float().cpu().numpy()
     T = -(-nT // S)
-    n_dis = 0
+    rec = Parity("mla_decode", lam)
     for b in units:
         qs, kvs = q[b:b + 1], kv[b:b + 1]
         ref = oracle.mla_decode(qs, kvs, d_latent=d_latent, scale=scale, lam=lam, num_splits=S)
         nd, row_dis = compare_decisions(mh[b:b + 1], gh[b:b + 1], ref.mask, ref.margin, lam)
-        n_dis += nd
+        rec.units += 1
+        rec.disagree += nd
+        rec.add_decisions(mh[b:b + 1], ref.mask, ref.margin, lam)
         for sp in range(S):
             tiles = list(range(sp * T, min(nT, sp * T + T)))
             assert ch[b, sp] == (int((mh[b, tiles] == 1).sum()) if tiles else 0)
@@ -242,10 +343,10 @@ def check_mla(q, kv, *, scale, lam, num_splits, units=None, d_latent=512):
                 assert ch[b, sp] == ref.counts[0, sp]
         over = oracle.mla_decode(qs, kvs, d_latent=d_latent, scale=scale, lam=lam, num_splits=S,
                                  mask_override=(mh[b:b + 1] == 1).astype(np.uint8))
-        check_output(og[b], over.o[0], f"mla sequence {b} under GPU mask")
+        rec.add_error(check_output(og_h[b], over.o[0], f"mla sequence {b} under GPU mask"), False)
         if not row_dis[0]:
-            check_output(og[b], ref.o[0], f"mla sequence {b}")
-    return n_dis
+            rec.add_error(check_output(og_h[b], ref.o[0], f"mla sequence {b}"), True)
+    return _finish(rec)
 
 
 def hot_prefill(B, Hq, Hkv, Lq, Lk, d, frac=0.2, seed=0, per_head_u=True):

@@ -190,16 +190,16 @@ def test_struct_layouts_match_the_header(capi, tmp_path):
     src.write_text(
         '#include <stdio.h>\n#include <stddef.h>\n#include "ssattn.h"\n'
         "int main(void) {\n"
-        '  printf("%zu %zu %zu %zu %zu\\n", sizeof(ss_debug_opts), sizeof(ss_problem),\n'
+        '  printf("%zu %zu %zu %zu %zu %zu\\n", sizeof(ss_debug_opts), sizeof(ss_problem),\n'
         "         offsetof(ss_debug_opts, fault_inject), offsetof(ss_problem, skip_counts),\n"
-        "         offsetof(ss_problem, stream));\n"
+        "         offsetof(ss_problem, stream), offsetof(ss_problem, fault_inject));\n"
         "  return 0;\n}\n")
     exe = tmp_path / "sz"
     subprocess.check_call(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)])
     got = [int(x) for x in subprocess.check_output([str(exe)], text=True).split()]
     want = [ctypes.sizeof(capi.ss_debug_opts), ctypes.sizeof(capi.ss_problem),
             capi.ss_debug_opts.fault_inject.offset, capi.ss_problem.skip_counts.offset,
-            capi.ss_problem.stream.offset]
+            capi.ss_problem.stream.offset, capi.ss_problem.fault_inject.offset]
     assert got == want
 
 
@@ -208,6 +208,16 @@ def test_workspace_size(capi):
     assert capi.ss_attn_decode_workspace_size(64, 32, 128, 8) == 64 * 32 * 8 * 130 * 4
     assert capi.ss_attn_mla_decode_workspace_size(64, 16, 512, 1) == 0
     assert capi.ss_attn_mla_decode_workspace_size(64, 16, 512, 16) == 64 * 16 * 16 * 514 * 4
+
+
+def test_static_scratch_size_matches_the_library(capi):
+    """The binding's copy of SS_DECODE_STATIC_SCRATCH_BYTES equals the size of
+    the array compiled into the library, and the header's define."""
+    src = open(HEADER).read()
+    m = re.search(r"#define SS_DECODE_STATIC_SCRATCH_BYTES \((\d+)u << (\d+)\)", src)
+    assert m, "define not found"
+    header = int(m.group(1)) << int(m.group(2))
+    assert capi.ss_decode_static_scratch_bytes() == header == capi.SS_DECODE_STATIC_SCRATCH_BYTES
 
 
 def test_product_does_not_import_the_oracle():

@@ -42,8 +42,15 @@ def test_prefill_calibration_hits_target_count(target):
     tol = _near(ref0.margin, ref0.mask, a, 2048)
     assert abs(int(res.counts.sum()) - k_want) <= tol
     assert abs(round(achieved * N) - k_want) <= tol
-    # both a's sit inside the same plateau of ln(lambda): same skipped count
+    # Both a's are the log-midpoint of the plateau of ln(lambda) that skips
+    # k_want tiles: the oracle's from its fp64 statistics, ss_calibrate's from
+    # the GPU's fp32 ones, whose ends differ by at most the statistic's error
+    # (the margin tolerance of the parity tests).  So the two midpoints agree
+    # to that error, and the oracle's own a skips exactly k_want tiles.
     assert a > 0 and a_orc > 0
+    assert abs(math.log(a) - math.log(a_orc)) <= 2e-2 + 2e-4 * abs(math.log(a_orc / 2048))
+    res_orc = oracle.prefill(inp.q, inp.k, inp.v, scale=scale, causal=True, lam=a_orc / 2048)
+    assert int(res_orc.counts.sum()) == k_want
 
 
 def test_decode_calibration_and_fit():

@@ -55,7 +55,7 @@ def make_paged(k, v, lens, spare_pages, seed):
 
 def check_paged(q, k, v, lens, *, scale, a, num_splits, spare_pages=3, seed=0):
     import oracle
-    from _parity import check_output, compare_decisions
+    from _parity import Parity, _finish, check_output, compare_decisions, guarded
     from block_sparse_attention_sm_gb300 import capi
 
     B, Hq, d = q.shape
@@ -66,19 +66,22 @@ def check_paged(q, k, v, lens, *, scale, a, num_splits, spare_pages=3, seed=0):
     seq_lens = torch.tensor(lens, dtype=torch.int32, device=q.device)
     ws_n = capi.ss_attn_decode_workspace_size(B, Hq, d, S)
     ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=q.device)
-    o = torch.full_like(q, float("nan"))
-    counts = torch.full((B * Hkv * S,), -1, dtype=torch.int32, device=q.device)
-    mask = torch.full((B * Hkv, max_pages), 7, dtype=torch.uint8, device=q.device)
-    margin = torch.full((B * Hkv, max_pages), 12345.0, dtype=torch.float32, device=q.device)
+    gbs = [guarded(q.shape, q.dtype, q.device, float("nan")),
+           guarded((B * Hkv * S,), torch.int32, q.device, -1),
+           guarded((B * Hkv, max_pages), torch.uint8, q.device, 7),
+           guarded((B * Hkv, max_pages), torch.float32, q.device, 12345.0)]
+    o, counts, mask, margin = (g.t for g in gbs)
     st = capi.ss_attn_decode_paged(q, kp, vp, table, seq_lens, o, B, Hq, Hkv, num_pages, max_pages,
                                    d, scale, a, S, counts, ws, ws_n, mask, margin)
     assert st == capi.SS_OK, capi.ss_status_string(st)
     assert capi.ss_stream_status() == capi.SS_OK
     torch.cuda.synchronize()
+    for g, what in zip(gbs, ("o", "skip_counts", "skip_mask", "vote_margin")):
+        g.check(what)
     og = o.float().cpu().numpy()
     mh, gh = mask.cpu().numpy(), margin.cpu().numpy()
     ch = counts.cpu().numpy().reshape(B * Hkv, S)
-    n_dis = 0
+    rec = Parity("decode_paged", a)
     for b, L in enumerate(lens):
         nT = -(-L // 128)
         T = -(-nT // S) if nT else 0
@@ -96,7 +99,9 @@ def check_paged(q, k, v, lens, *, scale, a, num_splits, spare_pages=3, seed=0):
             ref = oracle.decode(qs, ks, vs, scale=scale, lam=lam, num_splits=S)
             nd, row_dis = compare_decisions(mh[u:u + 1, :nT], gh[u:u + 1, :nT], ref.mask,
                                             ref.margin, lam)
-            n_dis += nd
+            rec.units += 1
+            rec.disagree += nd
+            rec.add_decisions(mh[u:u + 1, :nT], ref.mask, ref.margin, lam)
             for sp in range(S):
                 tiles = list(range(sp * T, min(nT, sp * T + T)))
                 assert ch[u, sp] == (int((mh[u, tiles] == 1).sum()) if tiles else 0)
@@ -104,10 +109,10 @@ def check_paged(q, k, v, lens, *, scale, a, num_splits, spare_pages=3, seed=0):
                     assert ch[u, sp] == ref.counts[0, sp]
             over = oracle.decode(qs, ks, vs, scale=scale, lam=lam, num_splits=S,
                                  mask_override=(mh[u:u + 1, :nT] == 1).astype(np.uint8))
-            check_output(rows, over.o[0], f"paged unit {u} under GPU mask")
+            rec.add_error(check_output(rows, over.o[0], f"paged unit {u} under GPU mask"), False)
             if not row_dis[0]:
-                check_output(rows, ref.o[0], f"paged unit {u}")
-    return n_dis
+                rec.add_error(check_output(rows, ref.o[0], f"paged unit {u}"), True)
+    return _finish(rec)
 
 
 CASES = [

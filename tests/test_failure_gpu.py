@@ -48,3 +48,24 @@ def test_expired_wait_reports_timeout_and_context_survives():
     assert capi.ss_stream_status() == capi.SS_OK
     check_decode(inp.q, inp.k, inp.v, scale=1 / math.sqrt(128), lam=0.002, num_splits=1)
     assert capi.ss_stream_status() == capi.SS_OK
+
+
+def test_calibration_reports_an_expired_wait():
+    """ss_calibrate reads the device status word after each count-only
+    launch: when a bounded wait expired (test-only fault_inject), the
+    counters are not used and it returns SS_ERR_TIMEOUT instead of an a."""
+    from _parity import hot_decode
+    from block_sparse_attention_sm_gb300 import capi
+
+    inp = hot_decode(1, 4, 1, 1024, 128, frac=0.2, seed=12)
+    counts = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert capi.ss_stream_status() == capi.SS_OK
+    prob = capi.ss_problem(capi.SS_DECODE, inp.q.data_ptr(), inp.k.data_ptr(), inp.v.data_ptr(),
+                           1, 4, 1, 1, 1024, 128, 1 / math.sqrt(128), 0, 1, counts.data_ptr(),
+                           capi._stream(None), 1)
+    st, _, _ = capi.ss_calibrate(prob, 0.5)
+    assert st == capi.SS_ERR_TIMEOUT
+    assert capi.ss_stream_status() == capi.SS_OK  # read and cleared by the calibration
+    prob.fault_inject = 0
+    st, a, achieved = capi.ss_calibrate(prob, 0.5)
+    assert st == capi.SS_OK and a > 0 and achieved > 0

@@ -127,7 +127,7 @@ def check_mla_paged(q, kv, lens, *, a, num_splits, spare_pages=3, seed=0):
     unused page and in the rows past a sequence's end) and compare each
     sequence with the oracle on its own rows."""
     import oracle
-    from _parity import check_output, compare_decisions
+    from _parity import Parity, _finish, check_output, compare_decisions, guarded
     from block_sparse_attention_sm_gb300 import capi
 
     B, Hq, dk = q.shape
@@ -151,15 +151,19 @@ def check_mla_paged(q, kv, lens, *, a, num_splits, spare_pages=3, seed=0):
     lens_t = torch.tensor(lens, dtype=torch.int32, device=q.device)
     ws_n = capi.ss_attn_mla_decode_workspace_size(B, Hq, 512, S)
     ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=q.device)
-    o = torch.full((B, Hq, 512), float("nan"), dtype=q.dtype, device=q.device)
-    counts = torch.full((B * S,), -1, dtype=torch.int32, device=q.device)
-    mask = torch.full((B, max_pages), 7, dtype=torch.uint8, device=q.device)
-    margin = torch.full((B, max_pages), 12345.0, dtype=torch.float32, device=q.device)
+    gbs = [guarded((B, Hq, 512), q.dtype, q.device, float("nan")),
+           guarded((B * S,), torch.int32, q.device, -1),
+           guarded((B, max_pages), torch.uint8, q.device, 7),
+           guarded((B, max_pages), torch.float32, q.device, 12345.0)]
+    o, counts, mask, margin = (g.t for g in gbs)
     st = capi.ss_attn_mla_decode_paged(q, pages, table_t, lens_t, o, B, Hq, num_pages, max_pages,
                                        512, dk - 512, SCALE, a, S, counts, ws, ws_n, mask, margin)
     assert st == capi.SS_OK, capi.ss_status_string(st)
     assert capi.ss_stream_status() == capi.SS_OK
     torch.cuda.synchronize()
+    for g, what in zip(gbs, ("o", "skip_counts", "skip_mask", "vote_margin")):
+        g.check(what)
+    rec = Parity("mla_decode_paged", a)
     og = o.float().cpu().numpy()
     mh, gh = mask.cpu().numpy(), margin.cpu().numpy()
     ch = counts.cpu().numpy().reshape(B, S)
@@ -174,7 +178,11 @@ def check_mla_paged(q, kv, lens, *, a, num_splits, spare_pages=3, seed=0):
         T = -(-nT // S)
         qs, kvs = q[b:b + 1], kv[b:b + 1, :L]
         ref = oracle.mla_decode(qs, kvs, d_latent=512, scale=SCALE, lam=lam, num_splits=S)
-        _, row_dis = compare_decisions(mh[b:b + 1, :nT], gh[b:b + 1, :nT], ref.mask, ref.margin, lam)
+        nd, row_dis = compare_decisions(mh[b:b + 1, :nT], gh[b:b + 1, :nT], ref.mask, ref.margin,
+                                        lam)
+        rec.units += 1
+        rec.disagree += nd
+        rec.add_decisions(mh[b:b + 1, :nT], ref.mask, ref.margin, lam)
         for sp in range(S):
             tiles = list(range(sp * T, min(nT, sp * T + T)))
             assert ch[b, sp] == (int((mh[b, tiles] == 1).sum()) if tiles else 0)
@@ -182,9 +190,11 @@ def check_mla_paged(q, kv, lens, *, a, num_splits, spare_pages=3, seed=0):
                 assert ch[b, sp] == ref.counts[0, sp]
         over = oracle.mla_decode(qs, kvs, d_latent=512, scale=SCALE, lam=lam, num_splits=S,
                                  mask_override=(mh[b:b + 1, :nT] == 1).astype(np.uint8))
-        check_output(og[b], over.o[0], f"paged mla sequence {b} under GPU mask")
+        rec.add_error(check_output(og[b], over.o[0], f"paged mla sequence {b} under GPU mask"),
+                      False)
         if not row_dis[0]:
-            check_output(og[b], ref.o[0], f"paged mla sequence {b}")
+            rec.add_error(check_output(og[b], ref.o[0], f"paged mla sequence {b}"), True)
+    return _finish(rec)
 
 
 PAGED = [

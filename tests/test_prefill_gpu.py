@@ -98,17 +98,36 @@ def test_long_gap_between_kept_tiles(d):
     check_prefill(q, k, v, scale=d ** -0.5, causal=False, lam=1e-3)
 
 
+def _lambdas_on_critical_values(margins, n):
+    """n thresholds lambda = exp(c) placed exactly on vote statistics c < 0
+    of the oracle (spread over their range): each such tile sits at distance
+    0 from ln(lambda), inside the near-margin band, where the GPU's fp32
+    statistic may fall on either side."""
+    m = np.asarray(margins, dtype=np.float64).ravel()
+    c = np.sort(m[np.isfinite(m) & (m < -1e-3)])
+    assert c.size >= n
+    return [float(np.exp(c[int(i)])) for i in np.linspace(0, c.size - 1, n + 2)[1:-1]]
+
+
 def test_random_scores_many_decisions():
-    """Plain N(0,1) inputs (no planted structure): margins spread out, so many
-    tiles sit near the threshold -- exercises the near-margin accounting."""
+    """Plain N(0,1) inputs (no planted structure): margins spread out.  Three
+    thresholds sit exactly on critical values of the oracle's vote
+    statistic, so near-margin tiles are certain; their decisions may differ
+    and are counted (reported in the session summary), all others must agree."""
+    import oracle
     from _parity import check_prefill
 
     g = torch.Generator(device="cuda").manual_seed(5)
     q = torch.randn(1, 2, 512, 128, device="cuda", generator=g).to(torch.bfloat16)
     k = torch.randn(1, 2, 2048, 128, device="cuda", generator=g).to(torch.bfloat16)
     v = torch.randn(1, 2, 2048, 128, device="cuda", generator=g).to(torch.bfloat16)
-    for lam in (0.3, 0.7, 1.0):
-        check_prefill(q, k, v, scale=128 ** -0.5, causal=True, lam=lam)
+    # the vote statistics do not depend on lambda (property P): take them at lambda = 0
+    ref0 = oracle.prefill(q, k, v, scale=128 ** -0.5, causal=True, lam=0.0)
+    lams = _lambdas_on_critical_values(ref0.margin, 3) + [0.3, 1.0]
+    near = 0
+    for lam in lams:
+        near += check_prefill(q, k, v, scale=128 ** -0.5, causal=True, lam=lam).near
+    assert near >= 3
 
 
 def _sampled_units(B, Hq, nqb, heads, rng):
@@ -118,33 +137,3 @@ def _sampled_units(B, Hq, nqb, heads, rng):
         for qb in sorted({0, nqb - 1, *rng.choice(nqb, size=6, replace=False).tolist()}):
             units.append((0, int(h), int(qb)))
     return units
-
-
-@pytest.mark.slow
-@pytest.mark.parametrize("workload,a", [("dit_prefill_32k", 3.0), ("llama_prefill_16k", 2.0),
-                                        ("llama_chunked_prefill_2k_on_32k", 2.0)])
-def test_full_size_sampled(workload, a):
-    """Full-size workloads in the bench's launch configuration; the oracle
-    checks sampled query blocks (first, last, random) of a few heads."""
-    from _parity import check_prefill
-    from block_sparse_attention_sm_gb300 import synth
-
-    inp, cfg = synth.make(workload, seed=0, device="cuda")
-    rng = np.random.default_rng(11)
-    nqb = -(-cfg["Lq"] // 128)
-    heads = sorted(rng.choice(cfg["Hq"], size=4, replace=False).tolist())
-    units = _sampled_units(1, cfg["Hq"], nqb, heads, rng)
-    check_prefill(inp.q, inp.k, inp.v, scale=cfg["scale"], causal=cfg["causal"],
-                  lam=a / cfg["Lk"], units=units)
-
-
-@pytest.mark.slow
-def test_long_prefill_128k_sampled():
-    from _parity import check_prefill
-    from block_sparse_attention_sm_gb300 import synth
-
-    inp, cfg = synth.make("long_prefill_128k", seed=0, device="cuda")
-    nqb = cfg["Lq"] // 128
-    units = [(0, 5, nqb - 1), (0, 5, 3), (0, 30, nqb // 2)]
-    check_prefill(inp.q, inp.k, inp.v, scale=cfg["scale"], causal=True, lam=2.0 / cfg["Lk"],
-                  units=units)

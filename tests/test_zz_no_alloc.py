@@ -8,7 +8,9 @@ fixed device array inside the library instead.  The test calls it through the
 C ABI twice in a row (different inputs and lambda, so stale contents from the
 first call would show up in the second) and compares each result with the
 regular workspace entry point's, within the tolerance the parity tests use.
-It also checks that a problem too large for the built-in array is refused.
+It also checks that a problem too large for the built-in array is refused, and
+that one whose partials fill the array to within a few KB of its end gives
+the workspace entry point's result.
 """
 import math
 
@@ -80,3 +82,27 @@ def test_noalloc_rejects_problems_beyond_the_static_array():
     q = torch.empty(16, dtype=torch.bfloat16, device="cuda")  # never read: refused first
     st = capi.ss_attn_decode_noalloc(q, q, q, q, B, Hq, 8, 32768, d, 0.1, 0.01, S, None)
     assert st == capi.SS_ERR_WORKSPACE
+
+
+def test_noalloc_problem_just_below_the_limit():
+    """63 sequences x 32 heads x 16 splits of (128 + 2) fp32 partials =
+    16,773,120 bytes, 4 KB short of the 16 MiB array: accepted, and equal to
+    the workspace entry point."""
+    from block_sparse_attention_sm_gb300 import capi
+
+    B, Hq, Hkv, Lk, d, S = 63, 32, 8, 4096, 128, 16
+    need = capi.ss_attn_decode_workspace_size(B, Hq, d, S)
+    limit = capi.ss_decode_static_scratch_bytes()
+    assert need <= limit and limit - need <= 8192
+    inp = _inputs(B, Hq, Hkv, Lk, d, 2)
+    lam = 3.0 / Lk
+    ref_o, ref_counts = _with_workspace(capi, inp, lam, S)
+    o = torch.full_like(inp.q, float("nan"))
+    counts = torch.full((B * Hkv * S,), -1, dtype=torch.int32, device="cuda")
+    st = capi.ss_attn_decode_noalloc(inp.q, inp.k, inp.v, o, B, Hq, Hkv, Lk, d,
+                                     1.0 / math.sqrt(d), lam, S, counts)
+    assert st == capi.SS_OK, capi.ss_status_string(st)
+    assert capi.ss_stream_status() == capi.SS_OK
+    err = (o.float() - ref_o.float()).abs()
+    assert float(err.max()) <= MAX_ABS and float(err.mean()) <= MEAN_ABS
+    assert torch.equal(counts, ref_counts)
