@@ -7,9 +7,10 @@ One step = the whole hot path over one batch of synthetic inputs:
   * decode "llama_decode_32k": 64 sequences x Hq32/Hkv8, KV 32768, d128,
     8 KV splits, lambda calibrated to 70%.
 Both kernels are timed with CUDA events on the launching stream.  `value` is
-prefill executed TFLOP/s (QK^T on every evaluated tile + P.V on kept tiles);
-`decode` reports HBM GB/s on the bytes the algorithm moves (all of K, kept V,
-Q and O).  Inputs exceed the 129 MB L2 (no flush needed).  Speedups are
+prefill TFLOP/s on the algorithm's FLOPs (QK^T on every evaluated tile + P.V
+on kept tiles: the work the method executes); the MMA FLOPs the kernel
+actually issues are reported beside them.  `decode` reports HBM GB/s on the
+bytes the algorithm moves (all of K, kept V, Q and O).  Inputs exceed the 129 MB L2 (no flush needed).  Speedups are
 against the library's own lambda = 0 path on the same inputs.
 
 python bench.py [--gpus N --steps K --warmup W] [--impl reference]
@@ -25,6 +26,8 @@ import statistics
 import subprocess
 import sys
 import time
+
+import numpy as np
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
@@ -147,8 +150,37 @@ def job_rate(work_per_rank, ws, ms):
 
 
 def prefill_flops(B, Hq, nqb, nT_eval, kept, d):
-    """Executed FLOPs: Q K^T on every evaluated tile, P.V on kept tiles."""
+    """Algorithmic FLOPs: Q K^T on every evaluated tile, P.V on kept tiles."""
     return 2 * TILE * TILE * d * (nT_eval + kept)
+
+
+def prefill_mma_flops(nT_eval, kept, d):
+    """MMA FLOPs the prefill kernel issues: its vote pass runs Q K^T on every
+    evaluated tile, its compute pass Q K^T again and P.V on each kept tile."""
+    return 2 * TILE * TILE * d * (nT_eval + 2 * kept)
+
+
+def read_stream_gbs(dev, gib=4, reps=5):
+    """A read-only HBM stream measured in the same process: CUDA-event time of
+    a torch sum over a bf16 buffer of `gib` GiB (best of `reps`).  The decode
+    kernel is almost pure reads, which a read+write copy does not measure."""
+    import torch
+
+    x = torch.ones(gib << 29, dtype=torch.bfloat16, device=dev)
+    x.sum(dtype=torch.float32)
+    best = None
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        x.sum(dtype=torch.float32)
+        e1.record()
+        e1.synchronize()
+        ms = e0.elapsed_time(e1)
+        best = ms if best is None else min(best, ms)
+    nbytes = x.numel() * x.element_size()
+    del x
+    torch.cuda.empty_cache()
+    return nbytes / best / 1e6
 
 
 def run_native(args):
@@ -275,39 +307,64 @@ def run_native(args):
     gbs = job_rate(bytes_d, ws, ms_d) / 1e6
 
     # ---------------------------------------------------------------- end to end (host buffers)
+    # One e2e step is the same work as one timed step -- a prefill and a
+    # decode through the C ABI -- with each step's inputs copied in from
+    # pinned host memory and its outputs copied out.  Prefill's inputs are its
+    # q, k and v; decode's are the 64 new query tokens and the newest key and
+    # value row of every (sequence, KV head), appended into the KV cache that
+    # stays resident on the device between steps (loaded from the host once,
+    # before timing).  Steps are pipelined over two device buffer sets on
+    # three streams (copy in, compute, copy out): step i+1's copies overlap
+    # step i's kernels.  A buffer set is refilled only after the step that
+    # used it has been computed and copied out.
     e2e_steps = max(3, min(args.steps, 10))
-    # Steps are pipelined over two device buffer sets on three streams (copy in,
-    # compute, copy out): step i+1's inputs travel while step i computes.  Every
-    # step still copies its own inputs in from pinned host memory and its
-    # result out; a buffer set is refilled only after the step that used it has
-    # been computed and copied out.
     hq_, hk_, hv_ = (t_.cpu().pin_memory() for t_ in (q, k, v))
     ho_ = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for _ in range(2)]
-    h2d = sum(t_.numel() * t_.element_size() for t_ in (hq_, hk_, hv_))
-    d2h = ho_[0].numel() * ho_[0].element_size()
+    e_dk, e_dv = torch.empty_like(dk), torch.empty_like(dv)
+    e_dk.copy_(dk.cpu())  # the resident cache, uploaded from the host once
+    e_dv.copy_(dv.cpu())
+    h_dq = dq.cpu().pin_memory()
+    h_knew = dk[:, :, dLk - 1:dLk].cpu().pin_memory()  # the step's new key / value rows
+    h_vnew = dv[:, :, dLk - 1:dLk].cpu().pin_memory()
+    hdo_ = [torch.empty(do.shape, dtype=do.dtype, pin_memory=True) for _ in range(2)]
+    h2d = sum(t_.numel() * t_.element_size() for t_ in (hq_, hk_, hv_, h_dq, h_knew, h_vnew))
+    d2h = ho_[0].numel() * ho_[0].element_size() + hdo_[0].numel() * hdo_[0].element_size()
     bufs = [(q, k, v, o), tuple(torch.empty_like(t_) for t_ in (q, k, v, o))]
+    dbufs = [tuple(torch.empty_like(t_) for t_ in (dq, h_knew, h_vnew, do)) for _ in range(2)]
     s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
     ev_in, ev_done, ev_out = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
 
     def e2e_step(i):
         b = i % 2
         bq, bk, bv, bo = bufs[b]
+        eq, ekn, evn, eo = dbufs[b]
         s_in.wait_event(ev_done[b])  # the step two back has read this set's inputs
         with torch.cuda.stream(s_in):
             bq.copy_(hq_, non_blocking=True)
             bk.copy_(hk_, non_blocking=True)
             bv.copy_(hv_, non_blocking=True)
+            eq.copy_(h_dq, non_blocking=True)
+            ekn.copy_(h_knew, non_blocking=True)
+            evn.copy_(h_vnew, non_blocking=True)
         ev_in[b].record(s_in)
         s_cmp.wait_event(ev_in[b])
-        s_cmp.wait_event(ev_out[b])  # the step two back has copied this set's output out
+        s_cmp.wait_event(ev_out[b])  # the step two back has copied this set's outputs out
         st_ = capi.ss_attn_prefill(bq, bk, bv, bo, B, Hq, Hkv, Lq, Lk, d, pcfg["scale"], 0, lam_p,
                                    p_cnt, s_cmp.cuda_stream)
         if st_ != capi.SS_OK:
             raise SystemExit(f"ss_attn_prefill: {capi.ss_status_string(st_)}")
+        with torch.cuda.stream(s_cmp):  # append the new rows (in stream order with decode)
+            e_dk[:, :, dLk - 1:dLk].copy_(ekn)
+            e_dv[:, :, dLk - 1:dLk].copy_(evn)
+        st_ = capi.ss_attn_decode(eq, e_dk, e_dv, eo, dB, dHq, dHkv, dLk, dd, dcfg["scale"], lam_d,
+                                  S, d_cnt, wsb, wsn, s_cmp.cuda_stream)
+        if st_ != capi.SS_OK:
+            raise SystemExit(f"ss_attn_decode: {capi.ss_status_string(st_)}")
         ev_done[b].record(s_cmp)
         s_out.wait_event(ev_done[b])
         with torch.cuda.stream(s_out):
             ho_[b].copy_(bo, non_blocking=True)
+            hdo_[b].copy_(eo, non_blocking=True)
         ev_out[b].record(s_out)
 
     for i in range(2):
@@ -324,12 +381,49 @@ def run_native(args):
     torch.cuda.synchronize()
     ms_e2e = e0.elapsed_time(e1) / e2e_steps
     (ms_e2e,) = max_over_ranks([ms_e2e], ws, dev)
+    st = capi.ss_stream_status(sh)
+    if st != capi.SS_OK:
+        raise SystemExit(f"device status after the end-to-end steps: {capi.ss_status_string(st)}")
+    e2e_o_match = bool(torch.equal(ho_[(e2e_steps - 1) % 2], bufs[(e2e_steps - 1) % 2][3].cpu()))
+    del bufs, dbufs, e_dk, e_dv, hq_, hk_, hv_
+    torch.cuda.empty_cache()
+
+    # ---------------------------------------------------------------- outputs for the parity sample
+    # The timed configuration (plain entry points at the timed lambdas) and the
+    # debug call with skip masks and vote margins (same kernels, same result),
+    # outside the timed region.  The oracle side of the comparison runs in the
+    # CPU-baseline leg below.
+    p_mask = torch.empty((p_units, nT), dtype=torch.uint8, device=dev)
+    p_margin = torch.empty((p_units, nT), dtype=torch.float32, device=dev)
+    o_dbg = torch.empty_like(q)
+    cnt_dbg = torch.empty_like(p_cnt)
+    prefill_call(lam_p)
+    st = capi.ss_attn_prefill_ex(q, k, v, o_dbg, B, Hq, Hkv, Lq, Lk, d, pcfg["scale"], 0, lam_p,
+                                 cnt_dbg, p_mask, p_margin, stream=sh)
+    dnT_ = dnT
+    d_mask = torch.empty((dB * dHkv, dnT_), dtype=torch.uint8, device=dev)
+    d_margin = torch.empty((dB * dHkv, dnT_), dtype=torch.float32, device=dev)
+    do_dbg = torch.empty_like(do)
+    dcnt_dbg = torch.empty_like(d_cnt)
+    decode_call(lam_d)
+    st2 = capi.ss_attn_decode_ex(dq, dk, dv, do_dbg, dB, dHq, dHkv, dLk, dd, dcfg["scale"], lam_d,
+                                 S, dcnt_dbg, wsb, wsn, d_mask, d_margin, stream=sh)
+    if st != capi.SS_OK or st2 != capi.SS_OK or capi.ss_stream_status(sh) != capi.SS_OK:
+        raise SystemExit("debug launches failed")
+    debug_same = bool(torch.equal(o, o_dbg) and torch.equal(p_cnt, cnt_dbg)
+                      and torch.equal(do, do_dbg) and torch.equal(d_cnt, dcnt_dbg))
+    gpu_out = {"prefill": {"o": o, "counts": p_cnt, "mask": p_mask, "margin": p_margin},
+               "decode": {"o": do, "counts": d_cnt, "mask": d_mask, "margin": d_margin},
+               "debug_call_equals_timed_call": debug_same}
+
+    read_gbs = read_stream_gbs(dev)
 
     line = None
     if rank == 0:
         peak_t = peaks["bf16"]
         achieved_p = flops_p / ms_p / 1e9
         achieved_d = bytes_d / ms_d / 1e6
+        flops_mma = prefill_mma_flops(p_eval, p_kept, d)
         line = {
             "metric": METRIC,
             "value": round(tflops, 2),
@@ -362,8 +456,15 @@ def run_native(args):
                 "tokens_per_s": round(dB * ws / ms_d * 1e3, 1),
                 "bytes_per_launch": bytes_d, "partials_bytes_overhead": bytes_d_part,
             },
-            "prefill": {"ms": round(ms_p, 4), "tflops_executed": round(tflops, 2),
-                        "tflops_dense_equivalent": round(flops_dense_eq * ws / ms_p / 1e9, 2)},
+            "prefill": {"ms": round(ms_p, 4),
+                        "tflops_algorithmic": round(tflops, 2),
+                        "tflops_mma_issued": round(flops_mma * ws / ms_p / 1e9, 2),
+                        "mma_issued_frac_of_peak": round(flops_mma / ms_p / 1e9 / peak_t, 4),
+                        "tflops_dense_equivalent": round(flops_dense_eq * ws / ms_p / 1e9, 2),
+                        "flops_algorithmic": flops_p, "flops_mma_issued": flops_mma,
+                        "flops_note": "algorithmic = QK^T on every evaluated tile + P.V on kept "
+                                      "tiles; mma_issued adds the compute pass's second QK^T of "
+                                      "each kept tile"},
             "speedup_vs_dense": {"prefill": round(ms_p0 / ms_p, 3), "decode": round(ms_d0 / ms_d, 3),
                                  "prefill_dense_ms": round(ms_p0, 4),
                                  "decode_dense_ms": round(ms_d0, 4),
@@ -379,20 +480,31 @@ def run_native(args):
                 "unit": "GB/s", "frac": round(achieved_d / peaks["hbm"], 4),
                 "traffic": _traffic("decode", ["decode_sm103.cu", "ptx_sm103.cuh", "common.cuh"]),
                 "kernel": "decode_kernel<128,4,Sparse> + decode_merge_kernel",
-                "peak_kind": f"HBM copy ({peaks['src']})",
+                "peak_kind": f"HBM copy, read+write ({peaks['src']})",
+                "read_stream_gbs": round(read_gbs, 1),
+                "frac_of_read_stream": round(achieved_d / read_gbs, 4),
+                "read_stream_kind": "torch sum over 4 GiB bf16, CUDA events, best of 5, same process",
             },
             "clocks": clk,
             "e2e": {"value": round(job_rate(flops_p, ws, ms_e2e) / 1e9, 2), "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": round(ms_e2e, 4),
-                    "what": "prefill through the C ABI with pinned host buffers: H2D q,k,v + "
-                            "kernel + D2H o every step, steps pipelined over two device "
-                            "buffer sets (step i+1's copies overlap step i's kernel)"},
+                    "output_copied_back_matches_device": e2e_o_match,
+                    "what": "one prefill + one decode per step through the C ABI, like the timed "
+                            "step: H2D of prefill q,k,v and of decode's 64 query tokens and "
+                            "new K/V rows (appended into the device-resident KV cache), both "
+                            "kernels, D2H of both outputs; steps pipelined over two buffer sets. "
+                            "value = prefill's algorithmic FLOPs / the whole step's time "
+                            "(prefill + decode), comparable with ms_per_step"},
             "gpu_launches": args.steps * 3,
         }
-    # CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only)
+    # CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only); the
+    # same oracle results give the parity block against the GPU outputs.
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(q, k, v, pcfg, lam_p, args.cpu_seconds)
+        base, par = cpu_baseline(q, k, v, pcfg, lam_p, args.cpu_seconds, gpu_out,
+                                 decode=(dq, dk, dv, dcfg, lam_d))
+        line["cpu_baseline"] = base
+        line["parity"] = par
     if rank == 0:
         print(json.dumps(line))
     if ws > 1:
@@ -765,11 +877,49 @@ def run_suite(args):
         stability()
 
 
-def cpu_baseline(q, k, v, cfg, lam, seconds_budget):
-    """Time the fp64 oracle (as it stands) on whole query blocks of the
-    prefill workload; report executed TFLOP/s on the same FLOP count."""
-    import numpy as np
+def _parity_units(rng, n, k=6):
+    """First, last and k random indices of range(n), in that order."""
+    rest = [int(x) for x in rng.permutation(np.arange(1, max(1, n - 1)))[:k]] if n > 2 else []
+    return list(dict.fromkeys([0, n - 1] + rest))
 
+
+def _compare_unit(stats, g_mask, g_margin, g_count, g_o, res_mask, res_margin, res_count, res_o,
+                  lam):
+    """Fold one unit's GPU-vs-oracle comparison into `stats` (acceptance of the
+    parity tests: decisions exact outside the near-margin band, counts exact
+    and outputs within max-abs / mean-abs on units whose decisions agree)."""
+    ln_lam = math.log(lam) if lam > 0 else -math.inf
+    ev = res_mask != 2
+    near = ev & (np.abs(res_margin - ln_lam) < 1e-2)
+    dis = (g_mask.astype(np.int64) != res_mask.astype(np.int64))
+    stats["units"] += 1
+    stats["tiles"] += int(ev.sum())
+    stats["skipped"] += int((g_mask == 1).sum())
+    stats["near_margin_tiles"] += int(near.sum())
+    stats["near_margin_disagreements"] += int((dis & near).sum())
+    stats["other_disagreements"] += int((dis & ~near).sum())
+    if not dis.any():
+        stats["count_mismatches"] += int(np.any(np.asarray(g_count) != np.asarray(res_count)))
+        err = np.abs(g_o.astype(np.float64) - res_o)
+        stats["max_abs"] = max(stats["max_abs"], float(err.max(initial=0.0)))
+        stats["mean_abs"] = max(stats["mean_abs"], float(err.mean()) if err.size else 0.0)
+
+
+def _new_stats(lam):
+    return {"lambda": lam, "units": 0, "tiles": 0, "skipped": 0, "near_margin_tiles": 0,
+            "near_margin_disagreements": 0, "other_disagreements": 0, "count_mismatches": 0,
+            "max_abs": 0.0, "mean_abs": 0.0}
+
+
+def cpu_baseline(q, k, v, cfg, lam, seconds_budget, gpu_out=None, decode=None):
+    """Time the fp64 oracle (as it stands) on whole query blocks of the
+    prefill workload; report TFLOP/s on the same algorithmic FLOP count.
+
+    The same oracle results are compared with the GPU's outputs of the timed
+    launch (gpu_out: o, counters, skip mask and vote margins) on those query
+    blocks -- the first, the last, then random ones of head 0 -- and, with
+    `decode`, on eight sampled (sequence, KV head) units of the decode
+    workload; that comparison is returned as the parity block."""
     import oracle
 
     oracle.build()
@@ -782,12 +932,19 @@ def cpu_baseline(q, k, v, cfg, lam, seconds_budget):
     Lk = k.shape[2]
     nT = -(-Lk // TILE)
     d = q.shape[3]
+    nqb = q.shape[2] // TILE
+    rng = np.random.default_rng(2024)
+    order = _parity_units(rng, nqb, k=nqb)  # first, last, then the rest shuffled
+    gp = None
+    if gpu_out is not None:
+        gp = {key: (val.cpu().numpy() if key != "o" else val[0, h].float().cpu().numpy())
+              for key, val in gpu_out["prefill"].items()}
+    pstats = _new_stats(lam)
     # probe one unit per core to size the sample to the budget
     n = cores
     done_units, done_s, done_flops = 0, 0.0, 0.0
-    start_qb = 0
     while True:
-        units = np.arange(start_qb, start_qb + n) % (q.shape[2] // TILE)
+        units = np.array(order[done_units:done_units + n])
         t0 = time.time()
         res = oracle.prefill(qb_h, kb_h, vb_h, scale=cfg["scale"], causal=False, lam=lam,
                              units=units)
@@ -796,17 +953,50 @@ def cpu_baseline(q, k, v, cfg, lam, seconds_budget):
         done_flops += 2 * TILE * TILE * d * (len(units) * nT + kept)
         done_units += len(units)
         done_s += dt
-        start_qb += n
-        if done_s > seconds_budget * 0.5 or done_units >= q.shape[2] // TILE:
+        if gp is not None:
+            for i, qb in enumerate(units.tolist()):
+                gid = h * nqb + qb
+                _compare_unit(pstats, gp["mask"][gid], gp["margin"][gid], gp["counts"][gid],
+                              gp["o"][qb * TILE:(qb + 1) * TILE], res.mask[i], res.margin[i],
+                              res.counts[i], res.o[i], lam)
+        if done_s > seconds_budget * 0.5 or done_units >= nqb:
             break
         n = max(cores, int(n * max(1.0, (seconds_budget - done_s) / max(dt, 1e-3) * 0.8)))
-        n = min(n, q.shape[2] // TILE - done_units)
+        n = min(n, nqb - done_units)
         if n <= 0:
             break
-    return {"value": round(done_flops / done_s / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
+    base = {"value": round(done_flops / done_s / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
             "kind": "oracle",
-            "sample": f"{done_units} query blocks (128 rows x 32768 keys, head 0) of "
-                      f"{PREFILL} at the same lambda, {done_s:.1f} s wall"}
+            "sample": f"{done_units} query blocks (128 rows x 32768 keys, head 0: the first, "
+                      f"the last, then seeded random ones) of {PREFILL} at the same lambda, "
+                      f"{done_s:.1f} s wall"}
+    if gpu_out is None:
+        return base, None
+    par = {"prefill": pstats,
+           "debug_call_equals_timed_call": gpu_out["debug_call_equals_timed_call"],
+           "tolerance": {"max_abs": 2e-2, "mean_abs": 2e-3, "near_margin_log": 1e-2}}
+    if decode is not None:
+        dq, dk, dv, dcfg, lam_d = decode
+        dB, dHq, _ = dq.shape
+        dHkv = dk.shape[1]
+        G = dHq // dHkv
+        S = dcfg["num_splits"]
+        gd = {key: val.cpu().numpy() if key != "o" else val.float().cpu().numpy()
+              for key, val in gpu_out["decode"].items()}
+        dstats = _new_stats(lam_d)
+        for u in _parity_units(rng, dB * dHkv):
+            b, kvh = divmod(u, dHkv)
+            res = oracle.decode(dq[b:b + 1, kvh * G:(kvh + 1) * G], dk[b:b + 1, kvh:kvh + 1],
+                                dv[b:b + 1, kvh:kvh + 1], scale=dcfg["scale"], lam=lam_d,
+                                num_splits=S)
+            _compare_unit(dstats, gd["mask"][u], gd["margin"][u],
+                          gd["counts"].reshape(dB * dHkv, S)[u], gd["o"][b, kvh * G:(kvh + 1) * G],
+                          res.mask[0], res.margin[0], res.counts[0], res.o[0], lam_d)
+        par["decode"] = dstats
+    par["pass"] = all(st_["other_disagreements"] == 0 and st_["count_mismatches"] == 0
+                      and st_["max_abs"] <= 2e-2 and st_["mean_abs"] <= 2e-3
+                      for key, st_ in par.items() if key in ("prefill", "decode"))
+    return base, par
 
 
 def run_reference(args):

@@ -142,3 +142,38 @@ def test_reference_arm_line_on_the_host():
     assert d["cpu_baseline"]["cores"] == 2 and d["cpu_baseline"]["kind"] == "oracle"
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert d["e2e"]["value"] == d["value"]
+
+
+def test_bench_parity_bookkeeping():
+    """The bench's parity block (built in its CPU-baseline leg from the oracle
+    results it times) counts near-margin disagreements apart from others, and
+    compares counts and outputs only on units whose decisions agree."""
+    import numpy as np
+
+    import bench
+
+    lam = 0.01
+    ln = np.log(lam)
+    st = bench._new_stats(lam)
+    mask_o = np.array([0, 1, 1, 2], np.uint8)
+    margin_o = np.array([np.inf, ln - 0.5, ln - 0.005, np.nan])
+    o_ref = np.zeros((4, 8))
+    # unit 1: identical decisions, small output error
+    bench._compare_unit(st, mask_o.copy(), margin_o, [2], o_ref + 1e-3, mask_o, margin_o, [2],
+                        o_ref, lam)
+    # unit 2: the near-margin tile (third) kept by the GPU: counted, output not compared
+    g = mask_o.copy()
+    g[2] = 0
+    bench._compare_unit(st, g, margin_o, [1], o_ref + 1.0, mask_o, margin_o, [2], o_ref, lam)
+    assert st["units"] == 2 and st["tiles"] == 6 and st["near_margin_tiles"] == 2
+    assert st["near_margin_disagreements"] == 1 and st["other_disagreements"] == 0
+    assert st["count_mismatches"] == 0 and abs(st["max_abs"] - 1e-3) < 1e-12
+    # unit 3: a disagreement far from the margin is reported as such
+    g = mask_o.copy()
+    g[1] = 0
+    bench._compare_unit(st, g, margin_o, [1], o_ref, mask_o, margin_o, [2], o_ref, lam)
+    assert st["other_disagreements"] == 1
+    rng = np.random.default_rng(0)
+    u = bench._parity_units(rng, 10)
+    assert u[:2] == [0, 9] and len(u) == 8 and len(set(u)) == 8
+    assert bench._parity_units(rng, 1) == [0]
