@@ -43,7 +43,7 @@ class _Prefill(ctypes.Structure):
         ("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int),
         ("Lq", ctypes.c_int), ("Lk", ctypes.c_int), ("d", ctypes.c_int),
         ("scale", ctypes.c_double), ("causal", ctypes.c_int), ("lam", ctypes.c_double),
-        ("Bq", ctypes.c_int), ("Bk", ctypes.c_int),
+        ("Bq", ctypes.c_int), ("Bk", ctypes.c_int), ("dv", ctypes.c_int),
     ]
 
 
@@ -97,7 +97,7 @@ def _bits(x) -> np.ndarray:
 
 @dataclass
 class PrefillResult:
-    o: np.ndarray        # [n, Bq, d] fp64
+    o: np.ndarray        # [n, Bq, dv] fp64
     mask: np.ndarray     # [n, nT] uint8
     margin: np.ndarray   # [n, nT] fp64
     counts: np.ndarray   # [n] uint32
@@ -118,24 +118,31 @@ class DecodeResult:
 
 def prefill(q, k, v, *, scale: float, causal: bool, lam: float, Bq: int = 128, Bk: int = 128,
             units=None, mask_override=None) -> PrefillResult:
-    """Skip-softmax prefill over q [B,Hq,Lq,d], k/v [B,Hkv,Lk,d] (bf16)."""
+    """Skip-softmax prefill over q [B,Hq,Lq,d], k [B,Hkv,Lk,d], v [B,Hkv,Lk,dv]
+    (bf16; dv may differ from d, as in the unabsorbed form of multi-head latent
+    attention, which the BLASST summary lists among the supported kinds,
+    §Belangrijkste Bijdragen item 4).  o is [n, Bq, dv]."""
     qb, kb, vb = _bits(q), _bits(k), _bits(v)
     B, Hq, Lq, d = qb.shape
     _, Hkv, Lk, _ = kb.shape
+    dv = vb.shape[-1]
+    if vb.shape[:3] != kb.shape[:3]:
+        raise ValueError("prefill: v must be [B, Hkv, Lk, dv] like k")
     nqb = -(-Lq // Bq)
     nT = -(-Lk // Bk)
     if units is None:
         units = np.arange(B * Hq * nqb, dtype=np.int64)
     units = np.ascontiguousarray(np.asarray(units, dtype=np.int64))
     n = len(units)
-    o = np.zeros((n, Bq, d), np.float64)
+    o = np.zeros((n, Bq, dv), np.float64)
     mask = np.zeros((n, nT), np.uint8)
     margin = np.zeros((n, nT), np.float64)
     counts = np.zeros(n, np.uint32)
     ov = None
     if mask_override is not None:
         ov = np.ascontiguousarray(np.asarray(mask_override, dtype=np.uint8).reshape(n, nT))
-    prob = _Prefill(B, Hq, Hkv, Lq, Lk, d, float(scale), int(bool(causal)), float(lam), Bq, Bk)
+    prob = _Prefill(B, Hq, Hkv, Lq, Lk, d, float(scale), int(bool(causal)), float(lam), Bq, Bk,
+                    dv)
     rc = _get().orc_prefill(ctypes.byref(prob), _ptr(qb), _ptr(kb), _ptr(vb), _ptr(units), n,
                             _ptr(ov), _ptr(o), _ptr(mask), _ptr(margin), _ptr(counts))
     if rc != 0:

@@ -136,9 +136,10 @@ int orc_prefill(const orc_prefill_problem* p, const uint16_t* q, const uint16_t*
                 uint32_t* counts) {
   if (!p || !q || !k || !v) return -1;
   if (p->B < 1 || p->Hq < 1 || p->Hkv < 1 || p->Hq % p->Hkv != 0 || p->Lq < 1 || p->Lk < 1 ||
-      p->d < 1 || p->Bq < 1 || p->Bk < 1 || !(p->lambda >= 0.0) || p->lambda > 1.0)
+      p->d < 1 || p->dv < 0 || p->Bq < 1 || p->Bk < 1 || !(p->lambda >= 0.0) || p->lambda > 1.0)
     return -1;
-  const int G = p->Hq / p->Hkv, d = p->d, Bq = p->Bq, Bk = p->Bk;
+  /* dk: width of q and k rows; d: width of v rows and of O */
+  const int G = p->Hq / p->Hkv, dk = p->d, d = (p->dv > 0) ? p->dv : p->d, Bq = p->Bq, Bk = p->Bk;
   const int64_t nQB = ceil_div(p->Lq, Bq), nT = ceil_div(p->Lk, Bk);
   const int64_t total = (int64_t)p->B * p->Hq * nQB;
   if (units == NULL) n_units = total;
@@ -167,11 +168,11 @@ int orc_prefill(const orc_prefill_problem* p, const uint16_t* q, const uint16_t*
     state_reset(&st);
     for (int r = 0; r < rows; ++r) {
       const int64_t row = r0 + r;
-      qrows[r] = q + ((size_t)(b * p->Hq + h) * p->Lq + (size_t)row) * d;
+      qrows[r] = q + ((size_t)(b * p->Hq + h) * p->Lq + (size_t)row) * dk;
       last_vis[r] = p->causal ? row + off : (int64_t)p->Lk - 1;
       if (last_vis[r] > (int64_t)p->Lk - 1) last_vis[r] = p->Lk - 1;
     }
-    const uint16_t* kh = k + (size_t)(b * p->Hkv + kvh) * p->Lk * d;
+    const uint16_t* kh = k + (size_t)(b * p->Hkv + kvh) * p->Lk * dk;
     const uint16_t* vh = v + (size_t)(b * p->Hkv + kvh) * p->Lk * d;
     uint32_t skipped = 0;
 
@@ -183,7 +184,7 @@ int orc_prefill(const orc_prefill_problem* p, const uint16_t* q, const uint16_t*
       const int ov = have_ov ? mask_override[(size_t)i * nT + j] : 0;
       double c;
       const int dec =
-          tile_step(&st, qrows, last_vis, kh, d, vh, k0, nk, p->scale, ln_lambda, have_ov, ov, s, tmax, &c);
+          tile_step(&st, qrows, last_vis, kh, dk, vh, k0, nk, p->scale, ln_lambda, have_ov, ov, s, tmax, &c);
       if (dec == ORC_SKIPPED) ++skipped;
       if (mask) mask[(size_t)i * nT + j] = (uint8_t)dec;
       if (margin) margin[(size_t)i * nT + j] = c;

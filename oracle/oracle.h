@@ -36,18 +36,21 @@ extern "C" {
 enum { ORC_KEPT = 0, ORC_SKIPPED = 1, ORC_NOT_EVALUATED = 2 };
 
 typedef struct {
-  int B, Hq, Hkv, Lq, Lk, d;
+  int B, Hq, Hkv, Lq, Lk, d; /* d: width of q and k rows */
   double scale;   /* s = scale * q.k */
   int causal;     /* bottom-right aligned: key k visible to row r iff k <= r + (Lk - Lq) */
   double lambda;  /* skip iff exp(tile_max - running_max) < lambda; 0 = dense */
   int Bq, Bk;     /* query-block rows, key-tile size (128 and 128 on the GPU path) */
+  int dv;         /* width of v rows and of o; 0: the same as d (multi-head latent
+                     attention in its unabsorbed prefill form has wider keys than values) */
 } orc_prefill_problem;
 
 /*
  * Prefill.  A unit is one (b, h_q, query block); unit id
  * u = (b*Hq + h)*nQB + qb with nQB = ceil(Lq/Bq).  `units` lists the unit ids
- * to compute (NULL: all, in order).  Outputs are packed per listed unit:
- *   o      [n][Bq][d]   attention output (rows past Lq left at 0)
+ * to compute (NULL: all, in order).  q and k rows are d wide, v rows dv wide.
+ * Outputs are packed per listed unit:
+ *   o      [n][Bq][dv]  attention output (rows past Lq left at 0)
  *   mask   [n][nT]      ORC_KEPT / ORC_SKIPPED / ORC_NOT_EVALUATED, nT = ceil(Lk/Bk)
  *   margin [n][nT]      c_j = max over rows (tile_max - running_max), natural-log
  *                       units; +INF when some row has no running max yet; NAN

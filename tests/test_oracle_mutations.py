@@ -46,6 +46,10 @@ MUTATIONS = {
     "decode_heads_interleaved": ("q + ((size_t)b * p->Hq + (size_t)kvh * G + g) * dk;",
                                  "q + ((size_t)b * p->Hq + (size_t)g * p->Hkv + kvh) * dk;"),
     "calib_lambda_above_one": ("if (hi > 0.0) hi = 0.0; /* lambda <= 1 */", ""),
+    # prefill with value rows of another width than query/key rows
+    "prefill_query_rows_value_width": ("(size_t)row) * dk;", "(size_t)row) * d;"),
+    "prefill_output_rows_key_width": ("double* ou = o + (size_t)i * Bq * d;\n      memset(ou, 0, sizeof(double) * (size_t)Bq * d);",
+                                      "double* ou = o + (size_t)i * Bq * dk;\n      memset(ou, 0, sizeof(double) * (size_t)Bq * d);"),
 }
 
 

@@ -414,6 +414,72 @@ def test_mla_sparse_decisions_and_output(oracle_lib, shape, lam):
         np.testing.assert_allclose(res.o[b], ref, rtol=0, atol=1e-10)
 
 
+# ------------------------------------------- prefill with wider keys than values
+# Multi-head latent attention (BLASST summary, §Belangrijkste Bijdragen item 4)
+# in its unabsorbed prefill form is attention whose query/key rows (latent
+# non-rotary + rotary parts) are wider than the value rows: d_qk != d_v.
+ASYM_SHAPES = [
+    # B, Hq, Hkv, Lq, Lk, dk, dv, causal, Bq, Bk
+    (1, 2, 2, 13, 29, 12, 8, True, 4, 4),
+    (1, 2, 1, 9, 17, 6, 10, False, 4, 5),    # values wider than keys, MQA
+    (1, 2, 2, 130, 260, 192, 128, True, 128, 128),  # the kernel's widths
+]
+
+
+def asym_case(oracle_lib, shape, lam, seed):
+    B, Hq, Hkv, Lq, Lk, dk, dv, causal, Bq, Bk = shape
+    rng = np.random.default_rng(seed)
+    u = rng.standard_normal(dk)
+    u /= np.linalg.norm(u)
+    q = rand_bits(rng, (B, Hq, Lq, dk), shift=3.0 * u)
+    kx = rng.standard_normal((B, Hkv, Lk, dk))
+    kx[rng.random((B, Hkv, Lk)) < 0.15] += 3.0 * u
+    k = bf16_bits(kx)
+    v = rand_bits(rng, (B, Hkv, Lk, dv))
+    scale = 1.0 / math.sqrt(dk)
+    res = oracle_lib.prefill(q, k, v, scale=scale, causal=causal, lam=lam, Bq=Bq, Bk=Bk)
+    return (q, k, v, scale), res
+
+
+@pytest.mark.parametrize("shape", ASYM_SHAPES)
+def test_prefill_value_width_dense_equals_two_pass(oracle_lib, shape):
+    """lambda = 0 with d_v != d_qk: o = softmax(scale q k^T) v over the
+    visible keys, computed directly (numpy, fp64)."""
+    B, Hq, Hkv, Lq, Lk, dk, dv, causal, Bq, Bk = shape
+    (q, k, v, scale), res = asym_case(oracle_lib, shape, 0.0, 31)
+    nqb = -(-Lq // Bq)
+    assert res.o.shape == (B * Hq * nqb, Bq, dv)
+    G = Hq // Hkv
+    vis = visible(Lq, Lk, causal)
+    for u in range(B * Hq * nqb):
+        b, h, r0, r1 = unit_rows(u, Hq, nqb, Bq, Lq)
+        ref = two_pass(f64(q[b, h]), f64(k[b, h // G]), f64(v[b, h // G]), scale, vis)
+        np.testing.assert_allclose(res.o[u, : r1 - r0], ref[r0:r1], rtol=0, atol=1e-10)
+
+
+@pytest.mark.parametrize("shape", ASYM_SHAPES)
+@pytest.mark.parametrize("lam", [0.05, 1.0])
+def test_prefill_value_width_sparse(oracle_lib, shape, lam):
+    """Decisions follow the prefix-maximum form over the key width alone (the
+    values play no part in them), and the output is the softmax restricted to
+    the kept tiles' keys with the dv-wide values."""
+    B, Hq, Hkv, Lq, Lk, dk, dv, causal, Bq, Bk = shape
+    (q, k, v, scale), res = asym_case(oracle_lib, shape, lam, 32)
+    nqb, nT = -(-Lq // Bq), -(-Lk // Bk)
+    G = Hq // Hkv
+    vis = visible(Lq, Lk, causal)
+    for u in range(B * Hq * nqb):
+        b, h, r0, r1 = unit_rows(u, Hq, nqb, Bq, Lq)
+        s = scale * (f64(q[b, h])[r0:r1] @ f64(k[b, h // G]).T)
+        s = np.where(vis[r0:r1], s, -np.inf)
+        m_ref, _ = prefix_decisions(s, Bk, range(nT), math.log(lam))
+        np.testing.assert_array_equal(res.mask[u], m_ref)
+        keep = np.repeat(res.mask[u] == 0, Bk)[:Lk]
+        ref = two_pass(f64(q[b, h])[r0:r1], f64(k[b, h // G]), f64(v[b, h // G]), scale,
+                       vis[r0:r1] & keep[None, :])
+        np.testing.assert_allclose(res.o[u, : r1 - r0], ref, rtol=0, atol=1e-10)
+
+
 # ------------------------------------------------------ worked examples
 def _decode_scalar(vals):
     return np.array([math.inf if x == "inf" else x for x in vals], dtype=np.float64)
