@@ -1,13 +1,17 @@
 """Build libssattn.so in-tree with nvcc for sm_103a (GB300).
 
 Each CUDA translation unit is compiled in parallel, then linked into one
-shared library next to this file.  Rebuilds only when a source or header is
-newer than the library.
+shared library next to this file.  Rebuilds when the library is missing or
+was built from other sources: a hash of every source, header and compiler
+flag is stored beside the library (``libssattn.so.sha256``), so a tree that
+arrives with a library built elsewhere, or with file times that do not
+reflect the edit order, is rebuilt rather than trusted.
 """
 from __future__ import annotations
 
 import concurrent.futures as cf
 import glob
+import hashlib
 import os
 import shutil
 import subprocess
@@ -36,16 +40,31 @@ def sources() -> list[str]:
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB):
+STAMP = LIB + ".sha256"
+
+
+def source_hash(extra_flags: list[str] | None = None) -> str:
+    """sha256 over the sources, headers, compiler flags and target."""
+    deps = sorted(sources() + glob.glob(os.path.join(CSRC, "*.cuh")) +
+                  glob.glob(os.path.join(INCLUDE, "*.h")))
+    h = hashlib.sha256()
+    for p in deps:
+        h.update(os.path.relpath(p, ROOT).encode())
+        h.update(open(p, "rb").read())
+    h.update(" ".join(ARCH + NVCC_FLAGS + list(extra_flags or [])).replace(ROOT, ".").encode())
+    return h.hexdigest()
+
+
+def _stale(extra_flags: list[str] | None = None) -> bool:
+    if not os.path.exists(LIB) or not os.path.exists(STAMP):
         return True
-    deps = sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h"))
-    return max(os.path.getmtime(p) for p in deps) > os.path.getmtime(LIB)
+    return open(STAMP).read().strip() != source_hash(extra_flags)
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None) -> str:
-    if not force and not _stale():
+    if not force and not _stale(extra_flags):
         return LIB
+    stamp = source_hash(extra_flags)
     nvcc = _nvcc()
     os.makedirs(BUILD_DIR, exist_ok=True)
     flags = NVCC_FLAGS + list(extra_flags or [])
@@ -68,6 +87,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
+    with open(STAMP, "w") as f:
+        f.write(stamp + "\n")
     return LIB
 
 

@@ -228,3 +228,22 @@ def test_product_does_not_import_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "oracle.h" not in text, f
+
+
+def test_rebuild_is_keyed_on_the_sources(capi):
+    """The library is rebuilt when its recorded source hash differs from the
+    tree's (a library built from other sources is never trusted because of
+    its file time)."""
+    from block_sparse_attention_sm_gb300 import builder
+
+    assert not builder._stale()
+    saved = open(builder.STAMP).read()
+    try:
+        with open(builder.STAMP, "w") as f:
+            f.write("0" * 64 + "\n")
+        assert builder._stale()
+    finally:
+        with open(builder.STAMP, "w") as f:
+            f.write(saved)
+    assert not builder._stale()
+    assert builder._stale(["-DSOMETHING_ELSE"])  # other flags, other library
