@@ -137,6 +137,36 @@ def prefill(q, k, v, *, scale: float, causal: bool = False, lam: float = 0.0, co
     return o
 
 
+def mla_prefill(q, k, v, *, scale: float, causal: bool = False, lam: float = 0.0, counts=None,
+                out=None, skip_mask=None, vote_margin=None, stream=None):
+    """Latent-attention prefill (unabsorbed form): q [B,Hq,Lq,192],
+    k [B,Hkv,Lk,192], v [B,Hkv,Lk,128] bf16 CUDA tensors.  Returns
+    o [B,Hq,Lq,128].  Counters and debug outputs as in :func:`prefill`."""
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _tensor(name, t, _bf16(), ndim=4)
+    B, Hq, Hkv, Lq, Lk, d = _shape_prefill(q, k)
+    dv = v.shape[3]
+    if tuple(v.shape[:3]) != tuple(k.shape[:3]):
+        raise ValueError("mla_prefill expects v [B,Hkv,Lk,d_v] with k's first three dims")
+    units = units_prefill(B, Hq, Lq)
+    _optional("counts", counts, _u32(), units)
+    _debug_outputs(skip_mask, vote_margin, units * math.ceil(Lk / TILE))
+    if out is not None:
+        _tensor("out", out, _bf16(), shape=(B, Hq, Lq, dv))
+    _on_cuda(q=q, k=k, v=v, out=out, counts=counts, skip_mask=skip_mask, vote_margin=vote_margin)
+    o = out if out is not None else torch.empty((B, Hq, Lq, dv), dtype=q.dtype, device=q.device)
+    if skip_mask is None and vote_margin is None:
+        st = capi.ss_attn_mla_prefill(q, k, v, o, B, Hq, Hkv, Lq, Lk, d, dv, scale, causal, lam,
+                                      counts, stream)
+    else:
+        st = capi.ss_attn_mla_prefill_ex(q, k, v, o, B, Hq, Hkv, Lq, Lk, d, dv, scale, causal,
+                                         lam, counts, skip_mask, vote_margin, False, stream)
+    _check(st, "ss_attn_mla_prefill")
+    return o
+
+
 def decode_workspace(B, Hq, d, num_kv_splits, device):
     import torch
 
@@ -232,20 +262,25 @@ def calibrate(kind: str, q, k, v, *, scale: float, target_sparsity: float, causa
               num_kv_splits: int = 1, counts=None, stream=None):
     """Fit a (lambda = a / Lk) for a target tile sparsity.  Returns (a, achieved).
 
-    kind: "prefill", "decode" or "mla_decode" (k is then the latent cache
-    [B,Lk,dk] and v is ignored)."""
+    kind: "prefill", "mla_prefill" (q/k 192 wide, v 128 wide), "decode" or
+    "mla_decode" (k is then the latent cache [B,Lk,dk] and v is ignored)."""
     import torch
 
-    if kind not in ("prefill", "decode", "mla_decode"):
+    if kind not in ("prefill", "decode", "mla_decode", "mla_prefill"):
         raise ValueError(f"calibrate: unknown kind {kind!r}")
-    _tensor("q", q, _bf16(), ndim=4 if kind == "prefill" else 3)
+    is_prefill = kind in ("prefill", "mla_prefill")
+    _tensor("q", q, _bf16(), ndim=4 if is_prefill else 3)
     _tensor("k", k, _bf16(), ndim=3 if kind == "mla_decode" else 4)
-    if kind != "mla_decode":
+    if kind == "mla_prefill":
+        _tensor("v", v, _bf16(), ndim=4)
+        if tuple(v.shape[:3]) != tuple(k.shape[:3]):
+            raise ValueError("mla_prefill expects v [B,Hkv,Lk,d_v] with k's first three dims")
+    elif kind != "mla_decode":
         _tensor("v", v, _bf16(), shape=k.shape)
-    if kind == "prefill":
+    if is_prefill:
         B, Hq, Hkv, Lq, Lk, d = _shape_prefill(q, k)
         n = units_prefill(B, Hq, Lq)
-        k_ = capi.SS_PREFILL
+        k_ = capi.SS_PREFILL if kind == "prefill" else capi.SS_MLA_PREFILL
     elif kind == "mla_decode":
         B, Hq, d = q.shape
         Lk = k.shape[1]

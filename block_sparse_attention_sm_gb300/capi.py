@@ -15,10 +15,11 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libssattn.so")
 
 SS_OK, SS_ERR_INVALID_ARG, SS_ERR_UNSUPPORTED, SS_ERR_CUDA, SS_ERR_TIMEOUT, SS_ERR_WORKSPACE = range(6)
-SS_PREFILL, SS_DECODE, SS_MLA_DECODE = 0, 1, 2
+SS_PREFILL, SS_DECODE, SS_MLA_DECODE, SS_MLA_PREFILL = 0, 1, 2, 3
 
 EXPORTS = (
-    "ss_attn_prefill", "ss_attn_prefill_ex", "ss_attn_decode_workspace_size", "ss_attn_decode",
+    "ss_attn_prefill", "ss_attn_prefill_ex", "ss_attn_mla_prefill", "ss_attn_mla_prefill_ex",
+    "ss_attn_decode_workspace_size", "ss_attn_decode",
     "ss_attn_decode_ex", "ss_attn_decode_noalloc", "ss_decode_static_scratch_bytes",
     "ss_attn_decode_paged",
     "ss_attn_mla_decode_workspace_size", "ss_attn_mla_decode", "ss_attn_mla_decode_ex",
@@ -64,6 +65,9 @@ def load() -> ctypes.CDLL:
     pre = [P, P, P, P, I, I, I, I, I, I, F, I, F, P]
     lib.ss_attn_prefill.argtypes = pre + [P]
     lib.ss_attn_prefill_ex.argtypes = pre + [ctypes.POINTER(ss_debug_opts), P]
+    mpre = [P, P, P, P, I, I, I, I, I, I, I, F, I, F, P]
+    lib.ss_attn_mla_prefill.argtypes = mpre + [P]
+    lib.ss_attn_mla_prefill_ex.argtypes = mpre + [ctypes.POINTER(ss_debug_opts), P]
     dec = [P, P, P, P, I, I, I, I, I, F, F, I, P, P, U]
     lib.ss_attn_decode.argtypes = dec + [P]
     lib.ss_attn_decode_ex.argtypes = dec + [ctypes.POINTER(ss_debug_opts), P]
@@ -89,7 +93,8 @@ def load() -> ctypes.CDLL:
     lib.ss_status_string.argtypes = [I]
     lib.ss_status_string.restype = ctypes.c_char_p
     lib.ss_stream_status.argtypes = [P]
-    for name in ("ss_attn_prefill", "ss_attn_prefill_ex", "ss_attn_decode", "ss_attn_decode_ex",
+    for name in ("ss_attn_prefill", "ss_attn_prefill_ex", "ss_attn_mla_prefill",
+                 "ss_attn_mla_prefill_ex", "ss_attn_decode", "ss_attn_decode_ex",
                  "ss_attn_decode_noalloc", "ss_attn_decode_paged", "ss_attn_mla_decode",
                  "ss_attn_mla_decode_ex", "ss_attn_mla_decode_paged", "ss_calibrate",
                  "ss_fit_factor", "ss_stream_status"):
@@ -139,6 +144,23 @@ def ss_attn_prefill_ex(q, k, v, o, B, Hq, Hkv, Lq, Lk, d, scale, causal, lam, sk
     return load().ss_attn_prefill_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, Hq, Hkv, Lq, Lk, d,
                                      float(scale), int(bool(causal)), float(lam),
                                      _ptr(skip_counts), ctypes.byref(dbg), _stream(stream))
+
+
+def ss_attn_mla_prefill(q, k, v, o, B, Hq, Hkv, Lq, Lk, d_qk, d_v, scale, causal, lam,
+                        skip_counts=None, stream=None) -> int:
+    """Latent-attention prefill: q/k rows d_qk wide, v/o rows d_v wide."""
+    return load().ss_attn_mla_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, Hq, Hkv, Lq, Lk,
+                                      d_qk, d_v, float(scale), int(bool(causal)), float(lam),
+                                      _ptr(skip_counts), _stream(stream))
+
+
+def ss_attn_mla_prefill_ex(q, k, v, o, B, Hq, Hkv, Lq, Lk, d_qk, d_v, scale, causal, lam,
+                           skip_counts=None, skip_mask=None, vote_margin=None, count_only=False,
+                           stream=None) -> int:
+    dbg = _dbg(skip_mask, vote_margin, count_only)
+    return load().ss_attn_mla_prefill_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, Hq, Hkv, Lq, Lk,
+                                         d_qk, d_v, float(scale), int(bool(causal)), float(lam),
+                                         _ptr(skip_counts), ctypes.byref(dbg), _stream(stream))
 
 
 def ss_attn_decode_workspace_size(B, Hq, d, num_kv_splits) -> int:

@@ -67,14 +67,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 3-D view [BH][L][d] of a bf16 tensor, 64 x 128 boxes, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, int d, int L, long BH) {
+// 3-D view [BH][L][d] of a bf16 tensor, 64 x box_rows boxes, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, int d, int L, long BH, int box_rows = kTile) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(L),
                         static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(L) * d * 2};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kTile), 1};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t es[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -91,9 +91,13 @@ float threshold_raw(double ln_lambda, float scale) {
   return static_cast<float>(ln_lambda / static_cast<double>(scale));
 }
 
+// d: width of q and k rows; dv: width of v and o rows (0: d).  Supported:
+// d = dv in {64, 128}, and d = 192 with dv = 128 (latent-attention prefill).
 ss_status prefill_impl(const void* q, const void* k, const void* v, void* o, int B, int Hq,
                        int Hkv, int Lq, int Lk, int d, float scale, int causal, bool dense,
-                       float thr_raw, uint32_t* counts, const ss_debug_opts* dbg, void* stream) {
+                       float thr_raw, uint32_t* counts, const ss_debug_opts* dbg, void* stream,
+                       int dv = 0) {
+  if (dv == 0) dv = d;
   const bool count_only = dbg != nullptr && dbg->count_only != 0;
   if (q == nullptr || k == nullptr || v == nullptr || (o == nullptr && !count_only))
     return SS_ERR_INVALID_ARG;
@@ -101,17 +105,29 @@ ss_status prefill_impl(const void* q, const void* k, const void* v, void* o, int
     return SS_ERR_INVALID_ARG;
   if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Lq < 1 || Lk < 1 || !scale_ok(scale))
     return SS_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return SS_ERR_UNSUPPORTED;
+  if (!((d == dv && (d == 64 || d == 128)) || (d == 192 && dv == 128))) return SS_ERR_UNSUPPORTED;
   const long nQB = ceil_div(Lq, kTile), nT = ceil_div(Lk, kTile);
   const long units = static_cast<long>(B) * Hq * nQB;
   if (units > 0x7fffffffL || static_cast<long>(B) * Hq > 0x7fffffffL) return SS_ERR_INVALID_ARG;
   ss_status st = check_device();
   if (st != SS_OK) return st;
 
+  // lambda = 0 with skip masks or margins requested runs the voting kernel with a
+  // threshold no tile passes (every tile kept, margins reported).
+  const bool debug_out = dbg != nullptr && (dbg->skip_mask != nullptr || dbg->vote_margin != nullptr);
+  const Mode mode =
+      count_only ? Mode::kCount : ((dense && !debug_out) ? Mode::kDense : Mode::kSparse);
+  // Which prefill kernel (both compute the one-pass definition):
+  //  - the CTA-pair kernel (two-SM MMAs, one pass) for the dense path at
+  //    d = 128 and for every mode at d_qk = 192 / d_v = 128;
+  //  - the one-CTA kernel (two query blocks per CTA; decisions of a run of
+  //    tiles first, kept tiles second) for voting and counting at d = 128
+  //    and for d = 64, where it measured faster.
+  const bool pair = (d == 192) || (d == 128 && mode == Mode::kDense);
   CUtensorMap tq, tk, tv;
   if (!make_map(&tq, q, d, Lq, static_cast<long>(B) * Hq) ||
-      !make_map(&tk, k, d, Lk, static_cast<long>(B) * Hkv) ||
-      !make_map(&tv, v, d, Lk, static_cast<long>(B) * Hkv))
+      !make_map(&tk, k, d, Lk, static_cast<long>(B) * Hkv, pair ? kTile / 2 : kTile) ||
+      !make_map(&tv, v, dv, Lk, static_cast<long>(B) * Hkv))
     return SS_ERR_CUDA;
 
   PrefillParams p{};
@@ -137,12 +153,8 @@ ss_status prefill_impl(const void* q, const void* k, const void* v, void* o, int
   p.mask = dbg ? dbg->skip_mask : nullptr;
   p.margin = dbg ? dbg->vote_margin : nullptr;
   p.status = status_ptr();
-  // lambda = 0 with skip masks or margins requested runs the voting kernel
-  // with a threshold no tile passes (every tile kept, margins reported).
-  const bool debug_out = p.mask != nullptr || p.margin != nullptr;
-  const Mode mode =
-      count_only ? Mode::kCount : ((dense && !debug_out) ? Mode::kDense : Mode::kSparse);
-  cudaError_t e = launch_prefill(d, mode, tq, tk, tv, p, static_cast<cudaStream_t>(stream));
+  cudaError_t e = pair ? launch_prefill_pair(d, mode, tq, tk, tv, p, static_cast<cudaStream_t>(stream))
+                       : launch_prefill(d, mode, tq, tk, tv, p, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
@@ -256,7 +268,7 @@ ss_status mla_impl(const void* q, const void* kv, void* o, int B, int Hq, int Lk
 // Evaluated (unit, tile) pairs of a problem (tiles a causal row block never
 // reaches are not evaluated).
 long evaluated_tiles(const ss_problem& p) {
-  const long nT = ceil_div(p.Lk, kTile);
+  const long nT = ceil_div(p.Lk, kTile);  // prefill kinds: SS_PREFILL, SS_MLA_PREFILL
   if (p.kind == SS_DECODE) return static_cast<long>(p.B) * p.Hkv * nT;
   if (p.kind == SS_MLA_DECODE) return static_cast<long>(p.B) * nT;
   const long nQB = ceil_div(p.Lq, kTile);
@@ -330,6 +342,25 @@ ss_status ss_attn_prefill(const void* q, const void* k, const void* v, void* o, 
                           uint32_t* skip_counts, void* stream) {
   return ss_attn_prefill_ex(q, k, v, o, B, Hq, Hkv, Lq, Lk, d, scale, causal, lambda, skip_counts,
                             nullptr, stream);
+}
+
+ss_status ss_attn_mla_prefill_ex(const void* q, const void* k, const void* v, void* o, int B,
+                                 int Hq, int Hkv, int Lq, int Lk, int d_qk, int d_v, float scale,
+                                 int causal, float lambda, uint32_t* skip_counts,
+                                 const ss_debug_opts* dbg, void* stream) {
+  if (!lambda_ok(lambda)) return SS_ERR_INVALID_ARG;
+  if (d_qk != 192 || d_v != 128) return SS_ERR_UNSUPPORTED;
+  const bool dense = lambda == 0.f;
+  const float thr = dense ? -INFINITY : threshold_raw(std::log(static_cast<double>(lambda)), scale);
+  return prefill_impl(q, k, v, o, B, Hq, Hkv, Lq, Lk, d_qk, scale, causal, dense, thr,
+                      skip_counts, dbg, stream, d_v);
+}
+
+ss_status ss_attn_mla_prefill(const void* q, const void* k, const void* v, void* o, int B, int Hq,
+                              int Hkv, int Lq, int Lk, int d_qk, int d_v, float scale, int causal,
+                              float lambda, uint32_t* skip_counts, void* stream) {
+  return ss_attn_mla_prefill_ex(q, k, v, o, B, Hq, Hkv, Lq, Lk, d_qk, d_v, scale, causal, lambda,
+                                skip_counts, nullptr, stream);
 }
 
 size_t ss_attn_decode_workspace_size(int B, int Hq, int d, int num_kv_splits) {
@@ -526,9 +557,11 @@ ss_status ss_calibrate(const ss_problem* p, float target_sparsity, float* a_out,
   if (p == nullptr || a_out == nullptr || p->skip_counts == nullptr || !aligned16(p->q) ||
       !(target_sparsity >= 0.f && target_sparsity <= 1.f) || p->Lk < 1)
     return SS_ERR_INVALID_ARG;
-  if (p->kind != SS_PREFILL && p->kind != SS_DECODE && p->kind != SS_MLA_DECODE)
+  if (p->kind != SS_PREFILL && p->kind != SS_DECODE && p->kind != SS_MLA_DECODE &&
+      p->kind != SS_MLA_PREFILL)
     return SS_ERR_INVALID_ARG;
   if (p->kind == SS_MLA_DECODE && (p->Hkv != 1 || p->d != kMlaDk)) return SS_ERR_UNSUPPORTED;
+  if (p->kind == SS_MLA_PREFILL && p->d != 192) return SS_ERR_UNSUPPORTED;
   const long N = evaluated_tiles(*p);
   const long ncnt = counter_len(*p);
   if (N <= 0 || ncnt <= 0) return SS_ERR_INVALID_ARG;
@@ -544,9 +577,10 @@ ss_status ss_calibrate(const ss_problem* p, float target_sparsity, float* a_out,
   auto count_at = [&](double ln_lambda, long* out) -> ss_status {
     const float thr = threshold_raw(ln_lambda, p->scale);
     ss_status st;
-    if (p->kind == SS_PREFILL)
+    if (p->kind == SS_PREFILL || p->kind == SS_MLA_PREFILL)
       st = prefill_impl(p->q, p->k, p->v, nullptr, p->B, p->Hq, p->Hkv, p->Lq, p->Lk, p->d,
-                        p->scale, p->causal, false, thr, p->skip_counts, &dbg, p->stream);
+                        p->scale, p->causal, false, thr, p->skip_counts, &dbg, p->stream,
+                        p->kind == SS_MLA_PREFILL ? 128 : 0);
     else if (p->kind == SS_MLA_DECODE)
       st = mla_impl(p->q, p->k, nullptr, p->B, p->Hq, p->Lk, kMlaLatent, kMlaRope, p->scale,
                     false, thr, p->num_kv_splits, p->skip_counts, nullptr, 0, &dbg, p->stream);

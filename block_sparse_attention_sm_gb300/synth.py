@@ -30,7 +30,7 @@ HOT_SHIFT = 12.0
 class Inputs:
     q: torch.Tensor          # prefill [B,Hq,Lq,d] / decode [B,Hq,d], bf16
     k: torch.Tensor          # [B,Hkv,Lk,d] bf16
-    v: torch.Tensor          # [B,Hkv,Lk,d] bf16
+    v: torch.Tensor          # [B,Hkv,Lk,dv] bf16 (dv = d except for latent-attention prefill)
     hot: np.ndarray          # [B,Hkv,nT] bool: which key tiles were made hot
     u: np.ndarray            # [Hkv,d] fp64 unit directions
 
@@ -64,10 +64,11 @@ def _randn(shape, seed: int, tensor_id: int, device) -> torch.Tensor:
     return torch.randn(shape, generator=g, device=device, dtype=torch.float32)
 
 
-def _keys_values(seed, B, Hkv, Lk, d, hot, u, device, shift):
+def _keys_values(seed, B, Hkv, Lk, d, hot, u, device, shift, dv=None):
     nT = -(-Lk // TILE)
+    dv = d if dv is None else dv
     k = torch.empty((B, Hkv, Lk, d), dtype=torch.bfloat16, device=device)
-    v = torch.empty((B, Hkv, Lk, d), dtype=torch.bfloat16, device=device)
+    v = torch.empty((B, Hkv, Lk, dv), dtype=torch.bfloat16, device=device)
     ut = torch.as_tensor(u, dtype=torch.float32, device=device)
     for b in range(B):  # per batch entry keeps the fp32 temporaries small
         kb = _randn((Hkv, Lk, d), seed * 100003 + b, 1, device)
@@ -79,14 +80,15 @@ def _keys_values(seed, B, Hkv, Lk, d, hot, u, device, shift):
             kb[h].index_add_(0, idx, (shift * ut[h]).expand(len(rows), d))
         k[b] = kb.to(torch.bfloat16)
         del kb
-        v[b] = _randn((Hkv, Lk, d), seed * 100003 + b, 2, device).to(torch.bfloat16)
+        v[b] = _randn((Hkv, Lk, dv), seed * 100003 + b, 2, device).to(torch.bfloat16)
     assert hot.shape[2] == nT
     return k, v
 
 
 def prefill_inputs(*, B, Hq, Hkv, Lq, Lk, d, hot_frac, seed=0, per_head_u=False,
-                   device="cpu", shift=HOT_SHIFT) -> Inputs:
-    """Prefill tensors q [B,Hq,Lq,d], k/v [B,Hkv,Lk,d] in bf16 on `device`."""
+                   device="cpu", shift=HOT_SHIFT, dv=None) -> Inputs:
+    """Prefill tensors q [B,Hq,Lq,d], k [B,Hkv,Lk,d], v [B,Hkv,Lk,dv] (dv = d
+    unless given) in bf16 on `device`."""
     G = Hq // Hkv
     nT = -(-Lk // TILE)
     hot = hot_tiles(seed, B, Hkv, nT, hot_frac)
@@ -98,7 +100,7 @@ def prefill_inputs(*, B, Hq, Hkv, Lq, Lk, d, hot_frac, seed=0, per_head_u=False,
         qb += shift * ut.repeat_interleave(G, dim=0)[:, None, :]
         q[b] = qb.to(torch.bfloat16)
         del qb
-    k, v = _keys_values(seed, B, Hkv, Lk, d, hot, u, device, shift)
+    k, v = _keys_values(seed, B, Hkv, Lk, d, hot, u, device, shift, dv)
     return Inputs(q, k, v, hot, u)
 
 
@@ -181,6 +183,11 @@ WORKLOADS = {
     # multi-query decode: 32 query heads on one KV head (a vote group of 32)
     "mqa_decode_32k": dict(kind="decode", B=64, Hq=32, Hkv=1, Lk=32768, d=128,
                            scale=128 ** -0.5, hot_frac=0.10, per_head_u=True, num_splits=8),
+    # latent-attention prefill in its unabsorbed form: per head 128 non-rotary
+    # + 64 rotary query/key entries and 128-wide values (DeepSeek-V2-Lite's 16
+    # heads), causal
+    "mla_prefill_16k": dict(kind="prefill", B=1, Hq=16, Hkv=16, Lq=16384, Lk=16384, d=192, dv=128,
+                            causal=True, scale=192 ** -0.5, hot_frac=0.10, per_head_u=True),
     "long_prefill_128k": dict(kind="prefill", B=1, Hq=32, Hkv=8, Lq=131072, Lk=131072, d=128,
                               causal=True, scale=128 ** -0.5, hot_frac=0.05, per_head_u=True),
     "long_decode_128k": dict(kind="decode", B=8, Hq=32, Hkv=8, Lk=131072, d=128,
@@ -199,7 +206,7 @@ def make(workload: str, seed: int = 0, device="cpu", **overrides) -> tuple[Input
     elif cfg["kind"] == "prefill":
         inp = prefill_inputs(B=cfg["B"], Hq=cfg["Hq"], Hkv=cfg["Hkv"], Lq=cfg["Lq"], Lk=cfg["Lk"],
                              d=cfg["d"], hot_frac=cfg["hot_frac"], seed=seed,
-                             per_head_u=cfg["per_head_u"], device=device)
+                             per_head_u=cfg["per_head_u"], device=device, dv=cfg.get("dv"))
     else:
         inp = decode_inputs(B=cfg["B"], Hq=cfg["Hq"], Hkv=cfg["Hkv"], Lk=cfg["Lk"], d=cfg["d"],
                             hot_frac=cfg["hot_frac"], seed=seed, per_head_u=cfg["per_head_u"],

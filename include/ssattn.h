@@ -61,8 +61,8 @@ typedef enum {
   SS_OK = 0,
   SS_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad shape, lambda or scale */
   SS_ERR_UNSUPPORTED = 2,  /* d not in {64,128}, decode with Hq/Hkv > 32, latent decode
-                              with other widths or Hq > 32, or the current device is not
-                              sm_103 */
+                              with other widths or Hq > 32, latent prefill with widths
+                              other than 192/128, or the current device is not sm_103 */
   SS_ERR_CUDA = 3,         /* a CUDA runtime call failed (launch, copy, sync) */
   SS_ERR_TIMEOUT = 4,      /* a kernel's bounded wait expired (logic error; reported, not hung) */
   SS_ERR_WORKSPACE = 5     /* decode workspace missing or too small */
@@ -114,6 +114,30 @@ ss_status ss_attn_prefill_ex(const void* q, const void* k, const void* v, void* 
                              int Hq, int Hkv, int Lq, int Lk, int d, float scale, int causal,
                              float lambda, uint32_t* skip_counts, const ss_debug_opts* dbg,
                              void* stream);
+
+/*
+ * Latent-attention (MLA) prefill: the skip test on multi-head latent
+ * attention in its unabsorbed prefill form, which the BLASST summary names
+ * among the attention kinds its prefill kernels support (§Belangrijkste
+ * Bijdragen, item 4: MHA, GQA, MQA and MLA).  Read as attention whose query
+ * and key rows (non-rotary latent projection followed by the rotary part) are
+ * wider than the value rows; the pages give no shapes, and the widths
+ * supported are DeepSeek-V2/V3's published ones: d_qk = 128 + 64 = 192,
+ * d_v = 128.  Everything else -- tiles, vote, causal alignment, GQA/MQA
+ * head map, counters, debug outputs -- is that of ss_attn_prefill.
+ *   q [B, Hq, Lq, d_qk], k [B, Hkv, Lk, d_qk], v [B, Hkv, Lk, d_v],
+ *   o [B, Hq, Lq, d_v]; bf16, contiguous, 16-byte aligned.
+ * Returns SS_OK, SS_ERR_INVALID_ARG, SS_ERR_UNSUPPORTED (other widths, or
+ * the current device is not sm_103) or SS_ERR_CUDA.
+ */
+ss_status ss_attn_mla_prefill(const void* q, const void* k, const void* v, void* o, int B, int Hq,
+                              int Hkv, int Lq, int Lk, int d_qk, int d_v, float scale, int causal,
+                              float lambda, uint32_t* skip_counts, void* stream);
+
+ss_status ss_attn_mla_prefill_ex(const void* q, const void* k, const void* v, void* o, int B,
+                                 int Hq, int Hkv, int Lq, int Lk, int d_qk, int d_v, float scale,
+                                 int causal, float lambda, uint32_t* skip_counts,
+                                 const ss_debug_opts* dbg, void* stream);
 
 /*
  * Bytes of device workspace ss_attn_decode needs for the per-split partial
@@ -295,7 +319,7 @@ ss_status ss_attn_mla_decode_paged(const void* q, const void* kv_pages, const in
                                    const ss_debug_opts* dbg, void* stream);
 
 /* A calibration problem: the inputs the threshold is fitted on. */
-typedef enum { SS_PREFILL = 0, SS_DECODE = 1, SS_MLA_DECODE = 2 } ss_kind;
+typedef enum { SS_PREFILL = 0, SS_DECODE = 1, SS_MLA_DECODE = 2, SS_MLA_PREFILL = 3 } ss_kind;
 typedef struct {
   ss_kind kind;
   const void* q;
@@ -309,7 +333,9 @@ typedef struct {
   int causal;      /* prefill only */
   int num_kv_splits; /* decode only */
   /* SS_MLA_DECODE: k is the latent cache [B][Lk][d], v is ignored, Hkv is 1
-     and d is the key width d_latent + d_rope (576, of which 512 latent). */
+     and d is the key width d_latent + d_rope (576, of which 512 latent).
+     SS_MLA_PREFILL: the tensors of ss_attn_mla_prefill, d = d_qk = 192 (the
+     values, 128 wide, are not read by the counting launches). */
   /* Device buffer for the per-unit counters, sized as the matching call's
      skip_counts (prefill: B*Hq*ceil(Lq/128); decode: B*Hkv*num_kv_splits;
      latent decode: B*num_kv_splits). */

@@ -147,25 +147,35 @@ def gpu_prefill_all(q, k, v, scale, causal, lam, chunk=0):
     (test-only option), so that short inputs take the multi-run path."""
     B, Hq, Lq, d = q.shape
     _, Hkv, Lk, _ = k.shape
+    dv = v.shape[-1]  # != d: latent-attention prefill (its own entry point)
     nqb, nT = -(-Lq // TILE), -(-Lk // TILE)
     n_units = B * Hq * nqb
     dev = q.device
-    og = guarded(q.shape, q.dtype, dev, float("nan"))
+    oshape = (B, Hq, Lq, dv)
+    og = guarded(oshape, q.dtype, dev, float("nan"))
     cg = guarded((n_units,), torch.int32, dev, -1)
     o, counts = og.t, cg.t
-    if chunk == 0:
+    if dv != d:
+        assert chunk == 0
+        st = capi.ss_attn_mla_prefill(q, k, v, o, B, Hq, Hkv, Lq, Lk, d, dv, scale, causal, lam,
+                                      counts)
+    elif chunk == 0:
         st = capi.ss_attn_prefill(q, k, v, o, B, Hq, Hkv, Lq, Lk, d, scale, causal, lam, counts)
     else:
         st = capi.ss_attn_prefill_ex(q, k, v, o, B, Hq, Hkv, Lq, Lk, d, scale, causal, lam,
                                      counts, vote_chunk_tiles=chunk)
     assert st == capi.SS_OK, capi.ss_status_string(st)
-    o2g = guarded(q.shape, q.dtype, dev, float("nan"))
+    o2g = guarded(oshape, q.dtype, dev, float("nan"))
     c2g = guarded((n_units,), torch.int32, dev, -1)
     mg = guarded((n_units, nT), torch.uint8, dev, 7)
     gg = guarded((n_units, nT), torch.float32, dev, 12345.0)
     o2, counts2, mask, margin = o2g.t, c2g.t, mg.t, gg.t
-    st = capi.ss_attn_prefill_ex(q, k, v, o2, B, Hq, Hkv, Lq, Lk, d, scale, causal, lam, counts2,
-                                 mask, margin, vote_chunk_tiles=chunk)
+    if dv != d:
+        st = capi.ss_attn_mla_prefill_ex(q, k, v, o2, B, Hq, Hkv, Lq, Lk, d, dv, scale, causal,
+                                         lam, counts2, mask, margin)
+    else:
+        st = capi.ss_attn_prefill_ex(q, k, v, o2, B, Hq, Hkv, Lq, Lk, d, scale, causal, lam,
+                                     counts2, mask, margin, vote_chunk_tiles=chunk)
     assert st == capi.SS_OK, capi.ss_status_string(st)
     assert capi.ss_stream_status() == capi.SS_OK
     torch.cuda.synchronize()
@@ -196,7 +206,7 @@ def check_prefill(q, k, v, *, scale, causal, lam, units=None, chunk=0) -> Parity
     by_head = {}
     for (b, h, qb) in units:
         by_head.setdefault((b, h), []).append(qb)
-    rec = Parity("prefill", lam)
+    rec = Parity("prefill" if v.shape[-1] == d else "mla_prefill", lam)
     counts_h = counts.cpu().numpy()
     mask_h = mask.cpu().numpy()
     margin_h = margin.cpu().numpy()
