@@ -106,10 +106,6 @@ struct DecodeParams {
 // Launchers (return a CUDA error code; arguments are already validated).
 cudaError_t launch_prefill(int d, Mode mode, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, const PrefillParams& p, cudaStream_t st);
-// Prefill on CTA pairs (two-SM MMAs); dqk = key width (128, or 192 with
-// 128-wide values).  tk must have 64-row boxes (each CTA loads half a tile).
-cudaError_t launch_prefill_pair(int dqk, Mode mode, const CUtensorMap& tq, const CUtensorMap& tk,
-                                const CUtensorMap& tv, const PrefillParams& p, cudaStream_t st);
 cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
                           Mode mode, cudaStream_t st);
 

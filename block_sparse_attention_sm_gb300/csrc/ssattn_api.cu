@@ -13,6 +13,12 @@
 
 namespace ssattn {
 
+// Prefill on CTA pairs (two-SM MMAs, prefill_pair_sm103.cu); dqk = key width
+// (128, or 192 with 128-wide values).  tk must have 64-row boxes (each CTA
+// loads half of a key tile).
+cudaError_t launch_prefill_pair(int dqk, Mode mode, const CUtensorMap& tq, const CUtensorMap& tk,
+                                const CUtensorMap& tv, const PrefillParams& p, cudaStream_t st);
+
 namespace {
 
 __device__ uint32_t g_device_status = 0;
