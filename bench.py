@@ -222,7 +222,7 @@ def run_native(args):
     o = torch.empty_like(q)
     p_cnt = torch.zeros(p_units, dtype=torch.int32, device=dev)
 
-    din, dcfg = synth.make(DECODE, seed=rank, device=dev,
+    din, dcfg = synth.make(args.decode_workload if args.profile else DECODE, seed=rank, device=dev,
                            **({"B": args.decode_batch} if args.decode_batch else {}))
     dq, dk, dv = din.q, din.k, din.v
     dB, dHq, dd = dq.shape
@@ -285,6 +285,8 @@ def run_native(args):
     # ---------------------------------------------------------------- timed region
     clocks = ClockSampler(local)
     clocks.start()
+    if args.profile and args.profile_dense:
+        lam_p, lam_d = 0.0, 0.0
     tp, td = timed_loop(lam_p, lam_d, args.steps, args.warmup)
     clk = clocks.stop()
     st = capi.ss_stream_status(sh)
@@ -554,7 +556,7 @@ def run_suite(args):
     import torch
 
     import block_sparse_attention_sm_gb300 as ss
-    from block_sparse_attention_sm_gb300 import synth
+    from block_sparse_attention_sm_gb300 import capi, synth
 
     ss.build()
     peaks = _peaks()
@@ -596,12 +598,25 @@ def run_suite(args):
             if s_t > 0 and a > 0:
                 fit_s.append(sk / n_eval)
                 fit_a.append(a)
+            # at d = 128 both prefill kernels run every mode: time each one
+            # explicitly beside the library's own choice
+            per_kernel = {}
+            if d == 128:
+                for kname, kid in (("one_cta", 1), ("pair", 2)):
+                    def run(kid=kid):
+                        st = capi.ss_attn_prefill_ex(q, k, v, o, B, Hq, k.shape[1], Lq, Lk, d,
+                                                     cfg["scale"], cfg["causal"], lam, cnt,
+                                                     prefill_kernel=kid)
+                        if st != 0:
+                            raise RuntimeError(capi.ss_status_string(st))
+                    per_kernel[kname] = round(_time_ms(run), 4)
             emit({"suite": name, "kind": "prefill", "target": s_t, "a": a, "lambda": lam,
                   "sparsity": round(sk / n_eval, 4), "ms": round(ms, 4),
                   "tflops_executed": round(flops / ms / 1e9, 1),
                   "tflops_dense_equivalent": round(dense_eq / ms / 1e9, 1),
                   "frac_of_peak": round(flops / ms / 1e9 / peaks["bf16"], 4),
-                  "speedup_vs_dense": round(dense_ms / ms, 3) if dense_ms else None})
+                  "speedup_vs_dense": round(dense_ms / ms, 3) if dense_ms else None,
+                  "ms_by_kernel": per_kernel or None})
         if len(fit_s) >= 2:
             A, Bc = ss.fit_factor(fit_s, fit_a)
             emit({"suite": name, "kind": "fit", "A": A, "B": Bc, "points": list(zip(fit_s, fit_a))})
@@ -1084,8 +1099,12 @@ def main():
                     help="measure every workload (calibrated sweeps, fits, stability); JSON lines")
     ap.add_argument("--profile", action="store_true",
                     help="run calibration + the timed loop only (for ncu); prints nothing")
+    ap.add_argument("--profile-dense", action="store_true",
+                    help="with --profile: run the timed loop at lambda = 0 (the dense path)")
     ap.add_argument("--prefill-heads", type=int, default=0,
                     help="profiling: shrink the prefill workload to this many heads")
+    ap.add_argument("--decode-workload", default=DECODE, choices=[DECODE, "mqa_decode_32k"],
+                    help="with --profile: the decode workload to run (multi-query: 32 heads on one KV head)")
     ap.add_argument("--decode-batch", type=int, default=0,
                     help="profiling: shrink the decode workload to this many sequences")
     ap.add_argument("--mla-batch", type=int, default=0,

@@ -37,7 +37,7 @@ class SSError(RuntimeError):
 class ss_debug_opts(ctypes.Structure):
     _fields_ = [("skip_mask", ctypes.c_void_p), ("vote_margin", ctypes.c_void_p),
                 ("count_only", ctypes.c_int), ("fault_inject", ctypes.c_int),
-                ("vote_chunk_tiles", ctypes.c_int)]
+                ("vote_chunk_tiles", ctypes.c_int), ("prefill_kernel", ctypes.c_int)]
 
 
 class ss_problem(ctypes.Structure):
@@ -121,9 +121,10 @@ def _stream(stream):
     return stream.cuda_stream
 
 
-def _dbg(skip_mask=None, vote_margin=None, count_only=False, fault_inject=0, vote_chunk_tiles=0):
+def _dbg(skip_mask=None, vote_margin=None, count_only=False, fault_inject=0, vote_chunk_tiles=0,
+         prefill_kernel=0):
     return ss_debug_opts(_ptr(skip_mask), _ptr(vote_margin), int(bool(count_only)),
-                         int(fault_inject), int(vote_chunk_tiles))
+                         int(fault_inject), int(vote_chunk_tiles), int(prefill_kernel))
 
 
 def ss_status_string(status: int) -> str:
@@ -139,8 +140,9 @@ def ss_attn_prefill(q, k, v, o, B, Hq, Hkv, Lq, Lk, d, scale, causal, lam, skip_
 
 def ss_attn_prefill_ex(q, k, v, o, B, Hq, Hkv, Lq, Lk, d, scale, causal, lam, skip_counts=None,
                        skip_mask=None, vote_margin=None, count_only=False, stream=None,
-                       vote_chunk_tiles=0) -> int:
-    dbg = _dbg(skip_mask, vote_margin, count_only, vote_chunk_tiles=vote_chunk_tiles)
+                       vote_chunk_tiles=0, prefill_kernel=0) -> int:
+    dbg = _dbg(skip_mask, vote_margin, count_only, vote_chunk_tiles=vote_chunk_tiles,
+               prefill_kernel=prefill_kernel)
     return load().ss_attn_prefill_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, Hq, Hkv, Lq, Lk, d,
                                      float(scale), int(bool(causal)), float(lam),
                                      _ptr(skip_counts), ctypes.byref(dbg), _stream(stream))

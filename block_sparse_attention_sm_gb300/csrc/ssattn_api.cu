@@ -129,7 +129,13 @@ ss_status prefill_impl(const void* q, const void* k, const void* v, void* o, int
   //  - the one-CTA kernel (two query blocks per CTA; decisions of a run of
   //    tiles first, kept tiles second) for voting and counting at d = 128
   //    and for d = 64, where it measured faster.
-  const bool pair = (d == 192) || (d == 128 && mode == Mode::kDense);
+  bool pair = (d == 192) || (d == 128 && mode == Mode::kDense);
+  const int which = dbg != nullptr ? dbg->prefill_kernel : 0;
+  if (which < 0 || which > 2) return SS_ERR_INVALID_ARG;
+  if (which != 0) {
+    if ((which == 1 && d == 192) || (which == 2 && d == 64)) return SS_ERR_UNSUPPORTED;
+    pair = (which == 2);
+  }
   CUtensorMap tq, tk, tv;
   if (!make_map(&tq, q, d, Lq, static_cast<long>(B) * Hq) ||
       !make_map(&tk, k, d, Lk, static_cast<long>(B) * Hkv, pair ? kTile / 2 : kTile) ||

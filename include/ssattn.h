@@ -96,6 +96,15 @@ typedef struct {
      [1, 2048] shortens the run so that short inputs take the multi-run
      path.  Results do not depend on it (up to rounding). */
   int vote_chunk_tiles;
+  /* Test and benchmark only, prefill only (0 otherwise).  The library has
+     two prefill kernels computing the same pass: 1 selects the one-CTA
+     kernel (two query blocks per CTA; the decisions of a run of tiles
+     first, kept tiles second), 2 the CTA-pair kernel (two-SM MMAs, one
+     pass).  0 chooses automatically (the pair kernel for the dense path at
+     d = 128, the one-CTA kernel for voting and counting at d = 128 and for
+     d = 64).  d = 64 has only the one-CTA kernel and d_qk = 192 only the pair
+     kernel: asking for the other returns SS_ERR_UNSUPPORTED. */
+  int prefill_kernel;
 } ss_debug_opts;
 
 /*

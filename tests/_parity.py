@@ -140,11 +140,13 @@ def check_output(o_gpu, o_ref, what=""):
     return mx, mean
 
 
-def gpu_prefill_all(q, k, v, scale, causal, lam, chunk=0):
+def gpu_prefill_all(q, k, v, scale, causal, lam, chunk=0, kernel=0):
     """Bench-configuration call (plain entry point) plus the debug call.
 
     chunk > 0: both calls use the debug entry point with that vote-run length
-    (test-only option), so that short inputs take the multi-run path."""
+    (test-only option), so that short inputs take the multi-run path.
+    kernel > 0: both calls use the debug entry point with that prefill kernel
+    (test-only option: 1 the one-CTA kernel, 2 the CTA-pair kernel)."""
     B, Hq, Lq, d = q.shape
     _, Hkv, Lk, _ = k.shape
     dv = v.shape[-1]  # != d: latent-attention prefill (its own entry point)
@@ -159,11 +161,11 @@ def gpu_prefill_all(q, k, v, scale, causal, lam, chunk=0):
         assert chunk == 0
         st = capi.ss_attn_mla_prefill(q, k, v, o, B, Hq, Hkv, Lq, Lk, d, dv, scale, causal, lam,
                                       counts)
-    elif chunk == 0:
+    elif chunk == 0 and kernel == 0:
         st = capi.ss_attn_prefill(q, k, v, o, B, Hq, Hkv, Lq, Lk, d, scale, causal, lam, counts)
     else:
         st = capi.ss_attn_prefill_ex(q, k, v, o, B, Hq, Hkv, Lq, Lk, d, scale, causal, lam,
-                                     counts, vote_chunk_tiles=chunk)
+                                     counts, vote_chunk_tiles=chunk, prefill_kernel=kernel)
     assert st == capi.SS_OK, capi.ss_status_string(st)
     o2g = guarded(oshape, q.dtype, dev, float("nan"))
     c2g = guarded((n_units,), torch.int32, dev, -1)
@@ -175,7 +177,8 @@ def gpu_prefill_all(q, k, v, scale, causal, lam, chunk=0):
                                          lam, counts2, mask, margin)
     else:
         st = capi.ss_attn_prefill_ex(q, k, v, o2, B, Hq, Hkv, Lq, Lk, d, scale, causal, lam,
-                                     counts2, mask, margin, vote_chunk_tiles=chunk)
+                                     counts2, mask, margin, vote_chunk_tiles=chunk,
+                                     prefill_kernel=kernel)
     assert st == capi.SS_OK, capi.ss_status_string(st)
     assert capi.ss_stream_status() == capi.SS_OK
     torch.cuda.synchronize()
@@ -194,13 +197,13 @@ def gpu_prefill_all(q, k, v, scale, causal, lam, chunk=0):
     return o, counts, mask, margin
 
 
-def check_prefill(q, k, v, *, scale, causal, lam, units=None, chunk=0) -> Parity:
+def check_prefill(q, k, v, *, scale, causal, lam, units=None, chunk=0, kernel=0) -> Parity:
     """Parity of one prefill launch; `units` = list of (b, h, qb) or None (all)."""
     B, Hq, Lq, d = q.shape
     _, Hkv, Lk, _ = k.shape
     G = Hq // Hkv
     nqb = -(-Lq // TILE)
-    o, counts, mask, margin = gpu_prefill_all(q, k, v, scale, causal, lam, chunk)
+    o, counts, mask, margin = gpu_prefill_all(q, k, v, scale, causal, lam, chunk, kernel)
     if units is None:
         units = [(b, h, qb) for b in range(B) for h in range(Hq) for qb in range(nqb)]
     by_head = {}

@@ -190,15 +190,17 @@ def test_struct_layouts_match_the_header(capi, tmp_path):
     src.write_text(
         '#include <stdio.h>\n#include <stddef.h>\n#include "ssattn.h"\n'
         "int main(void) {\n"
-        '  printf("%zu %zu %zu %zu %zu %zu\\n", sizeof(ss_debug_opts), sizeof(ss_problem),\n'
-        "         offsetof(ss_debug_opts, fault_inject), offsetof(ss_problem, skip_counts),\n"
+        '  printf("%zu %zu %zu %zu %zu %zu %zu\\n", sizeof(ss_debug_opts), sizeof(ss_problem),\n'
+        "         offsetof(ss_debug_opts, fault_inject), offsetof(ss_debug_opts, prefill_kernel),\n"
+        "         offsetof(ss_problem, skip_counts),\n"
         "         offsetof(ss_problem, stream), offsetof(ss_problem, fault_inject));\n"
         "  return 0;\n}\n")
     exe = tmp_path / "sz"
     subprocess.check_call(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)])
     got = [int(x) for x in subprocess.check_output([str(exe)], text=True).split()]
     want = [ctypes.sizeof(capi.ss_debug_opts), ctypes.sizeof(capi.ss_problem),
-            capi.ss_debug_opts.fault_inject.offset, capi.ss_problem.skip_counts.offset,
+            capi.ss_debug_opts.fault_inject.offset, capi.ss_debug_opts.prefill_kernel.offset,
+            capi.ss_problem.skip_counts.offset,
             capi.ss_problem.stream.offset, capi.ss_problem.fault_inject.offset]
     assert got == want
 
