@@ -55,6 +55,9 @@ def _src_hash(names):
     return h.hexdigest()[:16]
 
 
+PAIR_SOURCES = ["prefill_pair_sm103.cu", "ptx_pair_sm103.cuh", "ptx_sm103.cuh", "common.cuh"]
+
+
 def _traffic(kernel, sources):
     """DRAM bytes per launch from the committed ncu summary, if still current."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -154,10 +157,25 @@ def prefill_flops(B, Hq, nqb, nT_eval, kept, d):
     return 2 * TILE * TILE * d * (nT_eval + kept)
 
 
-def prefill_mma_flops(nT_eval, kept, d):
-    """MMA FLOPs the prefill kernel issues: its vote pass runs Q K^T on every
-    evaluated tile, its compute pass Q K^T again and P.V on each kept tile."""
-    return 2 * TILE * TILE * d * (nT_eval + 2 * kept)
+def prefill_mma_flops(nT_eval, pair_union_tiles, d):
+    """MMA FLOPs the CTA-pair prefill kernel issues: Q K^T once on every
+    evaluated tile, and P.V for both query blocks of a pair on every tile
+    that either block keeps (the pair's P.V covers both blocks; a block that
+    skipped the tile contributes zero rows).  `pair_union_tiles` counts, per
+    pair of query blocks, the tiles kept by either block."""
+    return 2 * TILE * TILE * d * (nT_eval + 2 * pair_union_tiles)
+
+
+def pair_union(mask, nqb):
+    """Tiles kept (mask 0) by either query block of each pair (blocks 2p and
+    2p + 1 of one head): mask is [B*Hq*nqb, nT] uint8 with units in
+    (b, h, query block) order.  A last, unpaired block counts alone."""
+    import torch
+
+    kept = (mask == 0).view(-1, nqb, mask.shape[1])
+    if nqb % 2:
+        kept = torch.cat([kept, torch.zeros_like(kept[:, :1])], dim=1)
+    return int((kept[:, 0::2] | kept[:, 1::2]).sum())
 
 
 def read_stream_gbs(dev, gib=4, reps=5):
@@ -435,7 +453,7 @@ def run_native(args):
         peak_t = peaks["bf16"]
         achieved_p = flops_p / ms_p / 1e9
         achieved_d = bytes_d / ms_d / 1e6
-        flops_mma = prefill_mma_flops(p_eval, p_kept, d)
+        flops_mma = prefill_mma_flops(p_eval, pair_union(p_mask, nqb), d)
         line = {
             "metric": METRIC,
             "value": round(tflops, 2),
@@ -475,8 +493,9 @@ def run_native(args):
                         "tflops_dense_equivalent": round(flops_dense_eq * ws / ms_p / 1e9, 2),
                         "flops_algorithmic": flops_p, "flops_mma_issued": flops_mma,
                         "flops_note": "algorithmic = QK^T on every evaluated tile + P.V on kept "
-                                      "tiles; mma_issued adds the compute pass's second QK^T of "
-                                      "each kept tile"},
+                                      "tiles; mma_issued = what the CTA-pair kernel runs: QK^T on "
+                                      "every evaluated tile, P.V for both blocks of a pair on every "
+                                      "tile either block keeps"},
             "speedup_vs_dense": {"prefill": round(ms_p0 / ms_p, 3), "decode": round(ms_d0 / ms_d, 3),
                                  "prefill_dense_ms": round(ms_p0, 4),
                                  "decode_dense_ms": round(ms_d0, 4),
@@ -484,8 +503,9 @@ def run_native(args):
             "roofline": {
                 "bound": "tensor", "achieved": round(achieved_p, 2), "peak": peak_t,
                 "unit": "TFLOP/s", "frac": round(achieved_p / peak_t, 4),
-                "traffic": _traffic("prefill", ["prefill_sm103.cu", "ptx_sm103.cuh", "common.cuh"]),
-                "kernel": "prefill_kernel<128,Sparse>", "peak_kind": f"bf16 burst ({peaks['src']})",
+                "traffic": _traffic("prefill_pair", PAIR_SOURCES),
+                "kernel": "prefill_pair_kernel<128,128,Sparse>",
+                "peak_kind": f"bf16 burst ({peaks['src']})",
             },
             "roofline_decode": {
                 "bound": "hbm", "achieved": round(achieved_d, 1), "peak": peaks["hbm"],

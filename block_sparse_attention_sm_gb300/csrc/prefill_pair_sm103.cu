@@ -17,33 +17,35 @@
 // tile decides and exponentiates.
 //
 // One pass, every tile once.  Per tile j, in each CTA:
-//   softmax warps 0-7 (two threads per query row: warp w has TMEM lanes
-//   32 (w % 4) .. + 31 and the score columns of half w / 4) load S_j, mask
-//   it, take each half's maximum and vote with one bar.red.and over all 256
-//   threads against the exact running maximum (both halves of every row
-//   must pass; the halves' maxima meet through shared memory across that
-//   barrier); a kept tile updates the running maximum and computes
-//   P = exp2((S - m_ref) * scale * log2e), a skipped one zeros (the pair's
-//   P.V covers both blocks and the other block may keep the tile); each
-//   half's P goes as bf16 pairs over the first 32 of the half's own score
-//   columns.  Each warp then publishes its decision: in CTA 0 by a store and
-//   an arrival on a local barrier, in CTA 1 by an asynchronous store into
-//   CTA 0 that completes 4 bytes on CTA 0's barrier (a plain remote store
-//   followed by a cluster-scope release would cost the warp a memory
-//   barrier, ~1400 cycles, on every tile).
+//   the softmax warpgroup j % 2 (warps 4 (j % 2) .. + 3, one thread per
+//   query row: warp w has TMEM lanes 32 (w % 4) .. + 31) loads S_j in two
+//   halves of 64 columns, masks it and takes each row's maximum; receives
+//   the rows' running state (exact maximum m, reference maximum m_ref) from
+//   the warpgroup that did tile j - 1; votes with one bar.red.and over its
+//   128 threads against m (every row must pass); hands the updated state on;
+//   and for a kept tile computes P = exp2((S - m_ref) * scale * log2e), for a
+//   skipped one zeros (the pair's P.V covers both blocks and the other block
+//   may keep the tile), as bf16 pairs over the first 32 columns of each
+//   half.  So the two warpgroups' work overlaps: one exponentiates while the
+//   other loads and votes, and only the short state hand-over is serial
+//   from tile to tile.  Each of the warpgroup's warps then publishes its
+//   decision: in CTA 0 by a store and an arrival on a local barrier, in CTA
+//   1 by an asynchronous store into CTA 0 that completes 4 bytes on CTA 0's
+//   barrier (a plain remote store followed by a cluster-scope release would
+//   cost the warp a memory barrier, ~1400 cycles, on every tile).
 //   In CTA 0 two threads issue the pair's MMAs: the P.V issuer waits for both
 //   blocks' decisions on tile j and, if either keeps it, issues O += P_j V_j
 //   (A = P from TMEM); then it frees the tile's score buffer for the score
 //   issuer, which issues S_{j+3} into it.  The P.V issuer passes a tcgen05
 //   fence before that barrier, which orders S_{j+3} after PV_j.
-// What bounds it (measured on sm_103a with microbenchmarks): one thread
-// issues two-SM M256 N128 K16 MMAs at the pipe's rate, 64 cycles each, in
-// any operand form; two threads issuing different kinds at once interleave
-// them at 88 cycles per step; and stores into TMEM by other warps (here P)
-// slow concurrent MMAs to ~88-99 cycles per step.  In this kernel the steps
-// average ~85 cycles, and the tile period is set by the two issuers' chain
-// PV_j -> S_{j+3}.  (With P in shared memory instead, or one issuer, the
-// kernel measured slower.)
+// What bounds it (measured on sm_103a): one thread issues two-SM M256 N128
+// K16 MMAs at the pipe's rate, 64 cycles each, in any operand form; two
+// threads issuing at once interleave at ~88 cycles per step, and TMEM loads
+// and stores by other warps slow concurrent MMAs further.  Here the steps
+// average ~85-95 cycles: with every softmax operation removed the dense
+// kernel still takes 93% of its time.  One issuer thread is slower (an MMA
+// issue waits for the pipe, so the thread cannot wait for decisions while
+// the pipe is busy), and so is P in shared memory (shared-memory bandwidth).
 // m_ref, the maximum P is referenced to, trails the exact maximum lazily: a
 // row moves it only when the exact maximum has grown by more than 2^8 in
 // exp2 units (so P stays below 256); the warps on such rows then ask the
@@ -52,7 +54,8 @@
 // fixed, kept tiles, counters and O are those of the one-pass definition.
 //
 // Roles (384 threads, 12 warps, in each CTA):
-//   warps 0-7  softmax and vote of this CTA's query block;
+//   warps 0-7  softmax and vote of this CTA's query block, as two
+//              warpgroups taking alternate tiles;
 //   warp 8     TMA producer of Q (once) and of this CTA's halves of K;
 //   warp 9     TMA producer of this CTA's halves of V;
 //   warp 10    TMEM allocation (both CTAs, two-SM form); in CTA 0 the issuer
@@ -72,12 +75,26 @@ namespace ssattn {
 namespace {
 
 constexpr float kRescaleLog2 = 8.0f;  // lazy-rescale slack (exp2 domain)
-constexpr int kSoftWarps = 8;                 // two per group of 32 rows: column halves
+constexpr int kSoftWarps = 8;                 // two warpgroups of 4: alternate tiles
+constexpr int kGroupWarps = 4;                // one thread per query row
 constexpr int kSoftThreads = 32 * kSoftWarps;
 constexpr int kThreads = kSoftThreads + 128;  // + producers and issuers
 constexpr int kWarpK = 8, kWarpV = 9, kWarpMma = 10, kWarpPV = 11;
 constexpr int kNB = 3;  // score buffers
 constexpr uint32_t kFlagKept = 1u, kFlagRescale = 2u;
+
+// Scheduling fence for registers: the 8 values `done` are complete before,
+// and the 16 values `next` are read only after, this point (a compiler hint
+// that bounds how far exponentials are hoisted ahead, and so the registers
+// they hold; no instruction is emitted).
+__device__ __forceinline__ void order_after(uint32_t* done, uint32_t* next) {
+  asm volatile(""
+               : "+r"(done[0]), "+r"(done[1]), "+r"(done[2]), "+r"(done[3]), "+r"(done[4]),
+                 "+r"(done[5]), "+r"(done[6]), "+r"(done[7]), "+r"(next[0]), "+r"(next[1]),
+                 "+r"(next[2]), "+r"(next[3]), "+r"(next[4]), "+r"(next[5]), "+r"(next[6]),
+                 "+r"(next[7]), "+r"(next[8]), "+r"(next[9]), "+r"(next[10]), "+r"(next[11]),
+                 "+r"(next[12]), "+r"(next[13]), "+r"(next[14]), "+r"(next[15]));
+}
 
 template <int DQK, int DV>
 struct PairCfg {
@@ -109,22 +126,22 @@ struct PairCtl {
   uint64_t k_empty[NK];        // each CTA: its K slot may be refilled
   uint64_t v_empty[NV];        // each CTA: its V slot may be refilled
   uint64_t s_full[kNB];        // each CTA: scores of the buffer's tile are in TMEM
-  uint64_t dec_local[kNB];     // leader: its 4 softmax warps have decided the buffer's tile
+  uint64_t dec_local[kNB];     // leader: the 4 warps on the buffer's tile have decided it
   uint64_t dec_peer[kNB];      // leader: CTA 1's 4 warps' decisions (16 bytes) have arrived
   uint64_t drain[kSoftWarps];  // each CTA, per softmax warp: the P.V MMAs issued so far are done
   uint64_t rescaled[2][kSoftWarps];  // leader: (CTA, warp) has rescaled its part of O
   uint64_t s_free[kNB];        // leader: the buffer's P.V is issued (or not needed)
   uint64_t o_full;             // each CTA: the last P.V is done
   uint64_t mma_done[2];        // leader: teardown, per issuer
-  alignas(16) uint32_t flags[kNB][kSoftWarps];       // leader: per buffer and softmax warp,
-                                                     // kFlagKept | kFlagRescale
-  alignas(16) uint32_t peer_flags[kNB][kSoftWarps];  // leader: the same for CTA 1's warps
+  alignas(16) uint32_t flags[kNB][kGroupWarps];       // leader: per buffer and warp of the
+                                                      // tile's warpgroup, kFlagKept | kFlagRescale
+  alignas(16) uint32_t peer_flags[kNB][kGroupWarps];  // leader: the same for CTA 1's warps
   uint32_t tmem_base;
   int abort_flag;
-  float red[2][kSoftWarps];
-  float xmax[2][2][kTile];  // per tile parity, column half and row: the half's maximum
-  uint32_t soft_fail[4];    // per period of 8 tiles (mod 4): some softmax thread failed a wait
-  float xsum[2][kTile];     // per column half and row: the half's softmax denominator
+  uint32_t skipped[2];         // per warpgroup: tiles it skipped
+  float red[2][kGroupWarps];   // per warpgroup and warp: largest vote statistic of a tile
+  float2 hand[kTile];          // per row: (m, m_ref) after the last tile, passed between warpgroups
+  float2 fin[2][kTile];        // per warpgroup and row: (m_ref, l) at the end
 };
 
 template <int DQK, int DV, Mode MODE>
@@ -197,7 +214,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < kNB; ++s) {
       mbar_init(&ctl->s_full[s], 1);
-      mbar_init(&ctl->dec_local[s], kSoftWarps);
+      mbar_init(&ctl->dec_local[s], kGroupWarps);
       mbar_init(&ctl->dec_peer[s], 1);
 
     }
@@ -284,9 +301,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         mma2_commit_mc(&ctl->s_full[bsel], 3);
         mma2_commit_mc(&ctl->k_empty[s], 3);
-        // CTA 1's softmax warps complete 4 bytes each on dec_peer for this
-        // tile; this arrival (the phase's one expected arrival) sets that count.
-        mbar_arrive_expect_tx(&ctl->dec_peer[bsel], 4 * kSoftWarps);
+        // CTA 1's four warps on this tile complete 4 bytes each on dec_peer;
+        // this arrival (the phase's one expected arrival) sets that count.
+        mbar_arrive_expect_tx(&ctl->dec_peer[bsel], 4 * kGroupWarps);
       }
       // Every MMA issued must have finished before TMEM is freed.
       mma2_commit_mc(&ctl->mma_done[0], 1);
@@ -300,7 +317,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t sVa = smem_u32(sV);
       bool ok = true;
       uint32_t o_acc = 0u;
-      uint32_t nresc = 0u;  // bit (kSoftWarps * r + w): parity of (CTA r, warp w)'s requests
+      uint32_t nresc = 0u;  // bit (kSoftWarps * r + warp): parity of (CTA r, warp)'s requests
       for (int j = 0; ok && j < n_pair; ++j) {
         const int bsel = j % kNB;
         const uint32_t ph = (j / kNB) & 1;
@@ -316,19 +333,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        uint32_t resc = 0u, any_kept = 0u;  // resc: bit (kSoftWarps * r + w)
+        // Tile j's decisions come from the warps of warpgroup j % 2.
+        const int wg0 = kGroupWarps * (j & 1);
+        uint32_t resc = 0u, any_kept = 0u;  // resc: bit (kGroupWarps * r + w)
         {
-          const volatile uint4* fl = reinterpret_cast<const volatile uint4*>(ctl->flags[bsel]);
-          const volatile uint4* gl = reinterpret_cast<const volatile uint4*>(ctl->peer_flags[bsel]);
-          const uint4 f0 = const_cast<const uint4&>(fl[0]), f1 = const_cast<const uint4&>(fl[1]);
-          const uint4 g0 = const_cast<const uint4&>(gl[0]), g1 = const_cast<const uint4&>(gl[1]);
-          const uint32_t f[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
-          const uint32_t g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+          // (plain loads: the barrier waits above are compiler memory barriers)
+          const uint4 f4 = *reinterpret_cast<const uint4*>(ctl->flags[bsel]);
+          const uint4 g4 = *reinterpret_cast<const uint4*>(ctl->peer_flags[bsel]);
+          const uint32_t f[4] = {f4.x, f4.y, f4.z, f4.w};
+          const uint32_t g[4] = {g4.x, g4.y, g4.z, g4.w};
 #pragma unroll
-          for (int w = 0; w < kSoftWarps; ++w) {
+          for (int w = 0; w < kGroupWarps; ++w) {
             any_kept |= (f[w] | g[w]) & kFlagKept;
             resc |= ((f[w] >> 1) & 1u) << w;
-            resc |= ((g[w] >> 1) & 1u) << (kSoftWarps + w);
+            resc |= ((g[w] >> 1) & 1u) << (kGroupWarps + w);
           }
         }
         if (kPV && resc) {
@@ -337,18 +355,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int r = 0; r < 2; ++r)
 #pragma unroll
-            for (int w = 0; w < kSoftWarps; ++w)
-              if (resc & (1u << (kSoftWarps * r + w)))
-                mma2_commit_mc(&ctl->drain[w], static_cast<uint16_t>(1u << r));
+            for (int w = 0; w < kGroupWarps; ++w)
+              if (resc & (1u << (kGroupWarps * r + w)))
+                mma2_commit_mc(&ctl->drain[wg0 + w], static_cast<uint16_t>(1u << r));
 #pragma unroll
           for (int r = 0; r < 2; ++r)
 #pragma unroll
-            for (int w = 0; w < kSoftWarps; ++w) {
-              const uint32_t bit = 1u << (kSoftWarps * r + w);
-              if (ok && (resc & bit)) {
+            for (int w = 0; w < kGroupWarps; ++w) {
+              const uint32_t bit = 1u << (kSoftWarps * r + wg0 + w);
+              if (ok && (resc & (1u << (kGroupWarps * r + w)))) {
                 const uint32_t par = (nresc & bit) ? 1u : 0u;
-                ok = (r == 0) ? mbar_wait_pair(&ctl->rescaled[0][w], par, abort_flag, peer_abort)
-                              : mbar_wait_pair<true>(&ctl->rescaled[1][w], par, abort_flag, peer_abort);
+                ok = (r == 0) ? mbar_wait_pair(&ctl->rescaled[0][wg0 + w], par, abort_flag, peer_abort)
+                              : mbar_wait_pair<true>(&ctl->rescaled[1][wg0 + w], par, abort_flag,
+                                                     peer_abort);
                 nresc ^= bit;
               }
             }
@@ -377,101 +396,145 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp < kSoftWarps) {
     // ------------------------------------------------------------ softmax / vote
-    // Two threads per query row: warp w reads TMEM lanes 32 (w % 4) .. + 31
-    // (its rows) and the score columns of half h = w / 4, and writes its P
-    // over the first half of those same columns (so no thread overwrites
-    // scores another thread still has to load).  A row's two halves meet
-    // through shared memory once per tile: at the vote (a barrier of all the
-    // softmax threads), or in the dense kernel at a barrier of the two warps
-    // that share the rows.  A failed wait does not leave the loop at once:
-    // the thread carries on (its later waits give up at once) until the next
-    // check, every 8 tiles, where all softmax threads leave together.
-    const int q4 = warp & 3, half = warp >> 2;
+    // Two warpgroups take alternate tiles: warpgroup g = warp / 4 handles the
+    // tiles j with j % 2 == g, one thread per query row (warp w reads TMEM
+    // lanes 32 (w % 4) .. + 31) over all 128 score columns, loaded as two
+    // halves of 64.  A row's running state passes from one warpgroup to the
+    // other once per tile: the warpgroup on tile j - 1 writes the exact running
+    // maximum m (the vote's reference) and the reference maximum m_ref of P to
+    // shared memory and arrives on a named barrier, and the warpgroup on tile j
+    // completes that barrier before its vote (one barrier per direction, so an
+    // arrival can only complete the hand-over it is meant for).  The state chain of consecutive
+    // tiles is therefore short (a barrier, the vote, a store), and each
+    // warpgroup's loads, maxima and exponentials overlap the other's.  Each
+    // warpgroup sums its own tiles' P into l against the m_ref it last saw; a
+    // moved m_ref rescales that sum when the state arrives, and the two sums
+    // meet at the end.  After a failed wait a thread carries on to the end of
+    // the loop (every later wait gives up at once), so all threads take the
+    // same sequence of named barriers.
+    const int g = warp / kGroupWarps, q4 = warp % kGroupWarps;
     const int row = q4 * 32 + lane;  // TMEM lane
+    const int gtid = tid - 128 * g;  // thread index within the warpgroup
     const long grow = static_cast<long>(r0_mine) + row;
     const bool row_valid = row < rows_mine;
     long lim = static_cast<long>(p.Lk) - 1;  // last key index this row may see
     if (p.causal && grow + off < lim) lim = grow + off;
     if (!row_valid) lim = -1;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(q4 * 32) << 16);
-    const uint32_t colO = lane_base + C::kColO + static_cast<uint32_t>(half * (DV / 2));
+    const uint32_t colO = lane_base + C::kColO;
     const float sl2 = p.scale_log2;
     const long unit = static_cast<long>(bh) * p.nQB + qb;
     const bool has_unit = rows_mine > 0;
-    float m_true = -INFINITY, m_ref = -INFINITY, l = 0.f;  // l: this half's keys
+    float m_true = -INFINITY, m_ref = -INFINITY, l = 0.f;
     uint32_t skipped = 0, n_drain = 0;
     bool ok = true;
     auto wwait = [&](uint64_t* bar, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, mbar_wait_pair(bar, parity, abort_flag, peer_abort));
     };
-    constexpr uint32_t kBar = 2;  // named barrier of all softmax threads
-    const uint32_t bar_pair = 3 + q4;  // named barrier of the two warps on these rows
+    constexpr uint32_t kBar = 2;               // named barrier of all softmax threads
+    const uint32_t bar_give = 3 + g;           // hand-over from this warpgroup
+    const uint32_t bar_take = 3 + (g ^ 1);     // hand-over to this warpgroup
+    const uint32_t bar_vote = 5 + g;           // the 128 threads of this warpgroup
 
-    for (int j = 0; j < n_pair; ++j) {
+    // Scores of keys 64 hf .. + 63 of tile j, masked, into sr; returns their maximum.
+    auto load_half = [&](uint32_t colS, int j, int hf, uint32_t* sr) -> float {
+      tmem_ld32p(colS + 64 * hf, sr);
+      tmem_ld32p(colS + 64 * hf + 32, sr + 32);
+      tmem_wait_ld();
+      const long k0 = static_cast<long>(j) * kTile + 64 * hf;
+      if (!(k0 + 63 <= lim)) {
+        const int vis = static_cast<int>(max(-1L, min(63L, lim - k0)));
+#pragma unroll
+        for (int e = 0; e < 64; ++e)
+          if (e > vis) sr[e] = __float_as_uint(-INFINITY);
+      }
+      float mx[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) mx[e] = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < 32; ++e)
+        mx[e & 3] = fmax3(mx[e & 3], __uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1]));
+      return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+    };
+    // P = exp2(s*scale*log2e - m_ref*scale*log2e) of the 64 scores in sr, as
+    // bf16 pairs into sr[0..31]; returns their sum.
+    auto exp_half = [&](uint32_t* sr) -> float {
+      const float mb = (m_ref == -INFINITY) ? 0.f : m_ref * sl2;
+      const uint64_t sl2x2 = f32x2(sl2, sl2), nmb = f32x2(-mb, -mb);
+      uint64_t ls[2] = {0ull, 0ull};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+#pragma unroll
+        for (int cc = 8 * q; cc < 8 * q + 8; ++cc) {
+          const uint64_t xp = fma_f32x2(
+              f32x2(__uint_as_float(sr[2 * cc]), __uint_as_float(sr[2 * cc + 1])), sl2x2, nmb);
+          const float p0 = ex2_approx(f32x2_lo(xp));
+          const float p1 = ex2_approx(f32x2_hi(xp));
+          ls[cc & 1] = add_f32x2(ls[cc & 1], f32x2(p0, p1));
+          sr[cc] = pack_bf16x2(p0, p1);
+        }
+        if (q < 3) order_after(sr + 8 * q, sr + 16 * (q + 1));
+      }
+      const uint64_t lsum = add_f32x2(ls[0], ls[1]);
+      return f32x2_lo(lsum) + f32x2_hi(lsum);
+    };
+
+    for (int j = g; j < n_pair; j += 2) {
       const int bsel = j % kNB;
       const uint32_t colS = lane_base + 128u * static_cast<uint32_t>(bsel);
-      const bool got = wwait(&ctl->s_full[bsel], (j / kNB) & 1);
-      if (!got) ok = false;
+      if (!wwait(&ctl->s_full[bsel], (j / kNB) & 1)) ok = false;
       tc_fence_after();
+      const bool mine = j < n_mine;
+      uint32_t sr[64];
+      float tmax = -INFINITY;
+      if (mine) {
+        tmax = load_half(colS, j, 0, sr);
+        // (finish the first half's maximum before the second half's load, so
+        // that only one half of the scores is ever held in registers)
+        asm volatile("" : "+f"(tmax));
+        tmax = fmaxf(tmax, load_half(colS, j, 1, sr));  // sr keeps the second half
+      }
+      // The state after tile j - 1, from the other warpgroup.
+      if (j > 0) {
+        named_bar_sync(bar_take, kSoftThreads);
+        const float2 hs = ctl->hand[row];
+        m_true = hs.x;
+        if (hs.y != m_ref) {
+          if (m_ref != -INFINITY) l *= ex2_approx((m_ref - hs.y) * sl2);
+          m_ref = hs.y;
+        }
+      }
       bool kept = false, resc = false;
       float alpha = 1.f;
-      uint32_t sr[64];
-      if (j < n_mine) {
-        // This half's 64 masked scores and their maximum.
-        tmem_ld32p(colS + 64 * half, sr);
-        tmem_ld32p(colS + 64 * half + 32, sr + 32);
-        tmem_wait_ld();
-        const long k0 = static_cast<long>(j) * kTile + 64 * half;
-        if (!(k0 + 63 <= lim)) {
-          const int vis = static_cast<int>(max(-1L, min(63L, lim - k0)));
-#pragma unroll
-          for (int e = 0; e < 64; ++e)
-            if (e > vis) sr[e] = __float_as_uint(-INFINITY);
-        }
-        float mx[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) mx[e] = -INFINITY;
-#pragma unroll
-        for (int e = 0; e < 32; ++e)
-          mx[e & 3] = fmax3(mx[e & 3], __uint_as_float(sr[2 * e]), __uint_as_float(sr[2 * e + 1]));
-        const float hmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-        ctl->xmax[j & 1][half][row] = hmax;
-        // Skip vote: every row must pass exp(scale*(tile_max - m)) < lambda,
-        // i.e. both halves of every row; a half with no visible key does not
-        // veto.
-        float c_h = -INFINITY;
-        if (hmax != -INFINITY) c_h = (m_true == -INFINITY) ? INFINITY : hmax - m_true;
+      if (mine) {
+        // Skip vote: every row of the block must pass exp(scale*(tile_max - m)) < lambda.
+        float c = -INFINITY;
+        if (tmax != -INFINITY) c = (m_true == -INFINITY) ? INFINITY : tmax - m_true;
         if constexpr (kVote) {
-          kept = !named_bar_and(kBar, kSoftThreads, c_h < p.thr_raw);
-        } else {
-          named_bar_sync(bar_pair, 64);
-          kept = true;
-        }
-        const float tmax = fmaxf(hmax, *reinterpret_cast<volatile float*>(&ctl->xmax[j & 1][half ^ 1][row]));
-        if constexpr (kVote) {
+          kept = !named_bar_and(bar_vote, 128, c < p.thr_raw);
           if (p.margin != nullptr) {
-            float cm = c_h;
+            float cm = c;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
-            if (lane == 0) *reinterpret_cast<volatile float*>(&ctl->red[j & 1][warp]) = cm;
-            named_bar_sync(kBar, kSoftThreads);
-            if (tid == 0 && has_unit) {
-              const volatile float* rr = ctl->red[j & 1];
-              float cmax = rr[0];
-#pragma unroll
-              for (int w = 1; w < kSoftWarps; ++w) cmax = fmaxf(cmax, rr[w]);
+            if (lane == 0) *reinterpret_cast<volatile float*>(&ctl->red[g][q4]) = cm;
+            named_bar_sync(bar_vote, 128);
+            if (gtid == 0 && has_unit) {
+              const volatile float* rr = ctl->red[g];
+              const float cmax = fmaxf(fmaxf(rr[0], rr[1]), fmaxf(rr[2], rr[3]));
               p.margin[unit * p.nT + j] = (cmax == INFINITY) ? INFINITY : cmax * p.scale;
             }
           }
-          if (tid == 0 && has_unit) {
+          if (gtid == 0 && has_unit) {
             skipped += kept ? 0u : 1u;
             if (p.mask != nullptr) p.mask[unit * p.nT + j] = kept ? 0 : 1;
           }
+        } else {
+          kept = true;
         }
         m_true = fmaxf(m_true, tmax);
         if (kPV && kept) {
-          // Both threads of a row hold the same maxima, so they take the same
-          // decisions; the two warps of a group of rows request rescales together.
+          // m_ref trails m lazily: it moves only when m has grown by more than
+          // 2^8 in exp2 units, and then the warp's rows of O are rescaled.
           bool need = false;
           if (m_ref == -INFINITY) {
             m_ref = m_true;  // no key of this row counted yet: its O row and l are zero
@@ -484,33 +547,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             l *= alpha;
             m_ref = m_true;
           }
-          // P = exp2(s*scale*log2e - m_ref*scale*log2e) as bf16 pairs.
-          const float mb = (m_ref == -INFINITY) ? 0.f : m_ref * sl2;
-          const uint64_t sl2x2 = f32x2(sl2, sl2), nmb = f32x2(-mb, -mb);
-          uint64_t ls[2] = {0ull, 0ull};
-#pragma unroll
-          for (int cc = 0; cc < 32; ++cc) {
-            const uint64_t xp = fma_f32x2(
-                f32x2(__uint_as_float(sr[2 * cc]), __uint_as_float(sr[2 * cc + 1])), sl2x2, nmb);
-            const float p0 = ex2_approx(f32x2_lo(xp));
-            const float p1 = ex2_approx(f32x2_hi(xp));
-            ls[cc & 1] = add_f32x2(ls[cc & 1], f32x2(p0, p1));
-            sr[cc] = pack_bf16x2(p0, p1);
-          }
-          const uint64_t lsum = add_f32x2(ls[0], ls[1]);
-          l += f32x2_lo(lsum) + f32x2_hi(lsum);
         }
       }
+      if (j + 1 < n_pair) {
+        ctl->hand[row] = make_float2(m_true, m_ref);
+        named_bar_arrive(bar_give, kSoftThreads);
+      }
       if constexpr (kPV) {
-        // P of this half's 64 keys as bf16 pairs over the first 32 of the
-        // half's own score columns (64*half ..): no other thread still has
-        // to load them.  A skipped or unseen tile writes zeros (the pair's
-        // P.V covers both blocks; the other block may keep the tile).
-        if (!kept) {
+        // P of keys 64 hf .. as bf16 pairs over the first 32 of those keys'
+        // own score columns (64 hf ..); the second half goes first, from the
+        // registers, then the first half is loaded again.  A skipped or unseen
+        // tile writes zeros (the pair's P.V covers both blocks; the other
+        // block may keep the tile).
+        if (kept) {
+          float ls = exp_half(sr);
+          tmem_st32p(colS + 64, sr);
+          load_half(colS, j, 0, sr);
+          ls += exp_half(sr);
+          tmem_st32p(colS, sr);
+          l += ls;
+        } else {
 #pragma unroll
           for (int e = 0; e < 32; ++e) sr[e] = 0u;
+          tmem_st32p(colS + 64, sr);
+          tmem_st32p(colS, sr);
         }
-        tmem_st32p(colS + 64 * half, sr);
         tmem_wait_st();
       }
       tc_fence_before();
@@ -518,22 +579,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         const uint32_t f = (kept ? kFlagKept : 0u) | (resc ? kFlagRescale : 0u);
         if (leader) {
-          *reinterpret_cast<volatile uint32_t*>(&ctl->flags[bsel][warp]) = f;
+          *reinterpret_cast<volatile uint32_t*>(&ctl->flags[bsel][q4]) = f;
           mbar_arrive(&ctl->dec_local[bsel]);
         } else {
-          st_async_u32(map_shared(smem_u32(&ctl->peer_flags[bsel][warp]), 0u), f,
+          st_async_u32(map_shared(smem_u32(&ctl->peer_flags[bsel][q4]), 0u), f,
                        lead(&ctl->dec_peer[bsel]));
         }
       }
       if (kPV && resc) {
         // The P.V issuer drains the P.V MMAs issued so far; then this warp's
-        // half of O on its 32 rows is rescaled before this tile's P.V.
+        // rows of O are rescaled before this tile's P.V.
         if (!wwait(&ctl->drain[warp], n_drain & 1)) ok = false;
         ++n_drain;
         if (ok) {
           tc_fence_after();
 #pragma unroll 1
-          for (int cc = 0; cc < DV / 64; ++cc) {
+          for (int cc = 0; cc < DV / 32; ++cc) {
             uint32_t orr[32];
             tmem_ld32p(colO + cc * 32, orr);
             tmem_wait_ld();
@@ -552,31 +613,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_arrive_cluster(lead(&ctl->rescaled[1][warp]));
         }
       }
-      // Every 8 tiles and at the last one, all softmax threads agree on
-      // failures and leave together.
-      if (((j & 7) == 7 || j + 1 == n_pair) && named_bar_or(kBar, kSoftThreads, !ok)) {
-        ok = false;
-        break;
-      }
     }
 
-    // The row's denominator: this half's sum plus the other half's.
-    ctl->xsum[half][row] = l;
+    // The row's denominator: both warpgroups' sums against the later m_ref
+    // (the one O is kept against).
+    ctl->fin[g][row] = make_float2(m_ref, l);
+    if (gtid == 0) ctl->skipped[g] = skipped;
     ok = !named_bar_or(kBar, kSoftThreads, !ok);
-    const float l_row = l + *reinterpret_cast<volatile float*>(&ctl->xsum[half ^ 1][row]);
+    const float2 other = ctl->fin[g ^ 1][row];
+    const float m_fin = fmaxf(m_ref, other.x);
+    float l_row = 0.f;
+    if (m_fin != -INFINITY) {
+      if (m_ref != -INFINITY) l_row += l * ex2_approx((m_ref - m_fin) * sl2);
+      if (other.x != -INFINITY) l_row += other.y * ex2_approx((other.x - m_fin) * sl2);
+    }
     if (kPV && ok && n_pair > 0) {
       ok = wwait(&ctl->o_full, 0);
       tc_fence_after();
     }
     if (kPV && ok && has_unit) {
-      // Epilogue: this half of O / l -> bf16 (a row that saw no key writes zeros).
+      // Epilogue: this warpgroup's half of the row's O / l -> bf16 (a row that
+      // saw no key writes zeros).
       const float inv_l = (l_row > 0.f) ? 1.f / l_row : 0.f;
-      __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * p.Lq + grow) * DV + half * (DV / 2);
+      __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * p.Lq + grow) * DV + g * (DV / 2);
 #pragma unroll 1
       for (int c = 0; c < DV / 64; ++c) {
         uint32_t orr[32];
         if (n_pair > 0) {
-          tmem_ld32p(colO + c * 32, orr);
+          tmem_ld32p(colO + g * (DV / 2) + c * 32, orr);
           tmem_wait_ld();
         } else {
 #pragma unroll
@@ -596,7 +660,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     }
     if (tid == 0 && has_unit) {
-      if (p.counts != nullptr) p.counts[unit] = skipped;
+      if (p.counts != nullptr) p.counts[unit] = ctl->skipped[0] + ctl->skipped[1];
       for (int j = n_mine; j < p.nT; ++j) {
         if (p.mask != nullptr) p.mask[unit * p.nT + j] = 2;
         if (p.margin != nullptr) p.margin[unit * p.nT + j] = NAN;

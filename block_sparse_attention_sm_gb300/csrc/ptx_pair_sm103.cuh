@@ -117,6 +117,13 @@ __device__ __forceinline__ bool mbar_wait_pair(uint64_t* bar, uint32_t parity,
   }
 }
 
+// Producer side of a named barrier: count this thread's arrival without
+// waiting.  Memory operations before it are visible to the threads that
+// complete the same phase with bar.sync.
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05, two SMs
 // Executed by one warp of EACH CTA of the pair: the allocation is made on
 // both SMs' tensor memory and its address written to each CTA's `smem_dst`.

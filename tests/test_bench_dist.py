@@ -177,3 +177,24 @@ def test_bench_parity_bookkeeping():
     u = bench._parity_units(rng, 10)
     assert u[:2] == [0, 9] and len(u) == 8 and len(set(u)) == 8
     assert bench._parity_units(rng, 1) == [0]
+
+
+def test_pair_union_counts_tiles_kept_by_either_block_of_a_pair():
+    """The MMA-issued FLOP count of the CTA-pair prefill kernel needs, per
+    pair of query blocks (2p, 2p + 1 of one head), the tiles either block
+    keeps; an unpaired last block counts alone."""
+    import torch
+
+    sys.path.insert(0, ROOT)
+    import bench
+
+    # 1 head, 3 query blocks (pair (0, 1) and block 2 alone), 4 tiles;
+    # mask values: 0 kept, 1 skipped, 2 not evaluated.
+    mask = torch.tensor([[0, 1, 1, 2],
+                         [1, 0, 1, 2],
+                         [0, 0, 1, 1]], dtype=torch.uint8)
+    assert bench.pair_union(mask, 3) == 2 + 2
+    # two heads of 2 blocks: union per head
+    mask2 = torch.tensor([[0, 1], [0, 1], [1, 1], [1, 0]], dtype=torch.uint8)
+    assert bench.pair_union(mask2, 2) == 1 + 1
+    assert bench.prefill_mma_flops(10, 3, 128) == 2 * 128 * 128 * 128 * (10 + 6)
