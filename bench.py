@@ -400,16 +400,22 @@ def run_native(args):
     for i in range(2):
         e2e_step(i)
     torch.cuda.synchronize()
-    barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(s_in)
-    for i in range(e2e_steps):
-        e2e_step(i)
-    s_out.wait_stream(s_cmp)
-    s_out.wait_stream(s_in)
-    e1.record(s_out)
-    torch.cuda.synchronize()
-    ms_e2e = e0.elapsed_time(e1) / e2e_steps
+    # The host<->device copies share the host's memory and link with other
+    # jobs on the machine, and a single run has shown copies stalled for
+    # ~10 ms: the e2e figure is the median of three timed runs (all reported).
+    e2e_runs = []
+    for _ in range(3):
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s_in)
+        for i in range(e2e_steps):
+            e2e_step(i)
+        s_out.wait_stream(s_cmp)
+        s_out.wait_stream(s_in)
+        e1.record(s_out)
+        torch.cuda.synchronize()
+        e2e_runs.append(e0.elapsed_time(e1) / e2e_steps)
+    ms_e2e = statistics.median(e2e_runs)
     (ms_e2e,) = max_over_ranks([ms_e2e], ws, dev)
     st = capi.ss_stream_status(sh)
     if st != capi.SS_OK:
@@ -524,13 +530,15 @@ def run_native(args):
             "e2e": {"value": round(job_rate(flops_p, ws, ms_e2e) / 1e9, 2), "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": round(ms_e2e, 4),
+                    "runs_ms_per_step": [round(x, 4) for x in e2e_runs],
                     "output_copied_back_matches_device": e2e_o_match,
                     "what": "one prefill + one decode per step through the C ABI, like the timed "
                             "step: H2D of prefill q,k,v and of decode's 64 query tokens and "
                             "new K/V rows (appended into the device-resident KV cache), both "
-                            "kernels, D2H of both outputs; steps pipelined over two buffer sets. "
-                            "value = prefill's algorithmic FLOPs / the whole step's time "
-                            "(prefill + decode), comparable with ms_per_step"},
+                            "kernels, D2H of both outputs; steps pipelined over two buffer sets "
+                            "(copies overlap the previous step's kernels). value = prefill's "
+                            "algorithmic FLOPs / the whole step's time (prefill + decode), "
+                            "comparable with ms_per_step; median of three timed runs"},
             "gpu_launches": args.steps * 3,
         }
     # CPU baseline: the oracle on a bounded sample (rank 0, N = 1 only); the
