@@ -925,6 +925,7 @@ def run_suite(args):
     if "mla" in parts:
         mla_points("mla_decode_32k", [0.0, 0.5, 0.7, 0.9])
         mla_points("mla_decode_32k_32h", [0.0, 0.7])
+        mla_points("mla_decode_32k_64h", [0.0, 0.7])
         mla_paged_points()
     if "sdpa" in parts:
         sdpa_points("dit_prefill_32k")

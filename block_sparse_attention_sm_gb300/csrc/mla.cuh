@@ -12,7 +12,9 @@ constexpr int kMlaLatent = 512;
 constexpr int kMlaRope = 64;
 constexpr int kMlaDk = kMlaLatent + kMlaRope;
 constexpr int kMlaNarrowHeads = 16;  // one softmax warpgroup (MMA N = 16) up to here
-constexpr int kMlaMaxHeads = 32;     // two softmax warpgroups (MMA N = 32)
+constexpr int kMlaWideHeads = 32;    // two softmax warpgroups (MMA N = 32) up to here
+constexpr int kMlaRowsMaxHeads = 64;  // heads as MMA rows, latent split over two CTAs
+constexpr int kMlaMaxHeads = kMlaRowsMaxHeads;
 
 struct MlaParams {
   int B, Hq, Lk;
@@ -42,6 +44,9 @@ cudaError_t launch_mla_decode(const CUtensorMap& tkv, const MlaParams& p, Mode m
                               cudaStream_t st);
 // Heads 17..32: the wide kernel (two softmax warpgroups of 16 heads each).
 cudaError_t launch_mla_decode_wide(const CUtensorMap& tkv, const MlaParams& p, Mode mode,
+                                   cudaStream_t st);
+// Heads 33..64: heads as the MMA rows, O's latent entries split over two CTAs.
+cudaError_t launch_mla_decode_rows(const CUtensorMap& tkv, const MlaParams& p, Mode mode,
                                    cudaStream_t st);
 // Log-sum-exp merge of the S > 1 partial states in p.part into p.o.
 cudaError_t launch_mla_merge(const MlaParams& p, cudaStream_t st);

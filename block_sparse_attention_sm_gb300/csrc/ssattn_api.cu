@@ -234,6 +234,13 @@ ss_status decode_impl(const void* q, const void* k, const void* v, void* o, int 
   return e == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
+// The latent-attention decode kernel for the number of heads.
+cudaError_t launch_mla_any(const CUtensorMap& tkv, const MlaParams& p, Mode mode, cudaStream_t st) {
+  if (p.Hq > kMlaWideHeads) return launch_mla_decode_rows(tkv, p, mode, st);
+  if (p.Hq > kMlaNarrowHeads) return launch_mla_decode_wide(tkv, p, mode, st);
+  return launch_mla_decode(tkv, p, mode, st);
+}
+
 size_t mla_ws(int B, int Hq, int d_latent, int S) {
   if (S <= 1 || B < 1 || Hq < 1 || d_latent < 1) return 0;
   return static_cast<size_t>(B) * Hq * S * (d_latent + 2) * sizeof(float);
@@ -277,9 +284,7 @@ ss_status mla_impl(const void* q, const void* kv, void* o, int B, int Hq, int Lk
   p.margin = dbg ? dbg->vote_margin : nullptr;
   p.status = status_ptr();
   const Mode mode = count_only ? Mode::kCount : (dense ? Mode::kDense : Mode::kSparse);
-  cudaError_t e = (Hq > kMlaNarrowHeads)
-                      ? launch_mla_decode_wide(tkv, p, mode, static_cast<cudaStream_t>(stream))
-                      : launch_mla_decode(tkv, p, mode, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_mla_any(tkv, p, mode, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 
@@ -455,9 +460,7 @@ ss_status ss_attn_mla_decode_paged(const void* q, const void* kv_pages, const in
   p.max_pages = max_pages;
   p.lambda_a = lambda_a;
   const Mode mode = count_only ? Mode::kCount : (lambda_a == 0.f ? Mode::kDense : Mode::kSparse);
-  cudaError_t e = (Hq > kMlaNarrowHeads)
-                      ? launch_mla_decode_wide(tkv, p, mode, static_cast<cudaStream_t>(stream))
-                      : launch_mla_decode(tkv, p, mode, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_mla_any(tkv, p, mode, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? SS_OK : SS_ERR_CUDA;
 }
 

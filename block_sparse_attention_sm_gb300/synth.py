@@ -180,6 +180,9 @@ WORKLOADS = {
     # the same with 32 query heads (DeepSeek-V3's 128 heads over 4 GPUs)
     "mla_decode_32k_32h": dict(kind="mla_decode", B=128, Hq=32, Lk=32768, d_latent=512,
                                d_rope=64, scale=192 ** -0.5, hot_frac=0.10, num_splits=4),
+    # the same with 64 query heads (DeepSeek-V3's 128 heads over 2 GPUs)
+    "mla_decode_32k_64h": dict(kind="mla_decode", B=128, Hq=64, Lk=32768, d_latent=512,
+                               d_rope=64, scale=192 ** -0.5, hot_frac=0.10, num_splits=4),
     # multi-query decode: 32 query heads on one KV head (a vote group of 32)
     "mqa_decode_32k": dict(kind="decode", B=64, Hq=32, Hkv=1, Lk=32768, d=128,
                            scale=128 ** -0.5, hot_frac=0.10, per_head_u=True, num_splits=8),

@@ -277,8 +277,10 @@ ss_status ss_attn_decode_noalloc(const void* q, const void* k_cache, const void*
  *   q:  [B][Hq][dk] bf16 (the absorbed queries), 16-byte aligned.
  *   kv: [B][Lk][dk] bf16 latent cache, contiguous, 16-byte aligned.
  *   o:  [B][Hq][d_latent] bf16.
- *   Only d_latent = 512, d_rope = 64 and 1 <= Hq <= 32 are supported (up to
- *   16 heads take one softmax warpgroup, 17..32 heads two).
+ *   Only d_latent = 512, d_rope = 64 and 1 <= Hq <= 64 are supported (up to
+ *   16 heads take one softmax warpgroup, 17..32 heads two; 33..64 heads run
+ *   with the heads as the rows of the MMAs and the latent entries of O split
+ *   over two CTAs per (sequence, split)).
  *   skip_counts: nullable device buffer [B*num_kv_splits]; overwritten.
  *   workspace: device buffer of at least
  *     ss_attn_mla_decode_workspace_size(B, Hq, d_latent, num_kv_splits)

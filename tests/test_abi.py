@@ -135,7 +135,7 @@ def test_paged_decode_rejects_before_launch(capi, kw, expect):
     (dict(S=0), "SS_ERR_INVALID_ARG"),
     (dict(lam=1.5), "SS_ERR_INVALID_ARG"),
     (dict(scale=0.0), "SS_ERR_INVALID_ARG"),
-    (dict(Hq=33), "SS_ERR_UNSUPPORTED"),            # voting group wider than two warpgroups
+    (dict(Hq=65), "SS_ERR_UNSUPPORTED"),            # more heads than one staged query block
     (dict(d_latent=256), "SS_ERR_UNSUPPORTED"),
     (dict(d_rope=32), "SS_ERR_UNSUPPORTED"),
     (dict(S=4, ws_bytes=16), "SS_ERR_WORKSPACE"),
@@ -158,7 +158,7 @@ def test_mla_decode_rejects_before_launch(capi, kw, expect):
     (dict(a=-1.0), "SS_ERR_INVALID_ARG"),
     (dict(a=float("inf")), "SS_ERR_INVALID_ARG"),
     (dict(kv=FAKE + 4), "SS_ERR_INVALID_ARG"),
-    (dict(Hq=33), "SS_ERR_UNSUPPORTED"),
+    (dict(Hq=65), "SS_ERR_UNSUPPORTED"),
     (dict(d_rope=32), "SS_ERR_UNSUPPORTED"),
     (dict(S=4, ws=None), "SS_ERR_WORKSPACE"),
 ])

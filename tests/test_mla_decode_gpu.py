@@ -45,6 +45,12 @@ CASES = [
     (3, 24, 5000, 3),     # heads padded to the MMA's 32 rows
     (2, 32, 4096, 8),     # both warpgroups full
     (1, 32, 20000, 2),    # long splits
+    # 33..64 heads: heads as the MMA rows, O's latent entries over two CTAs
+    (2, 33, 1000, 1),     # ragged last tile, one split (no merge)
+    (3, 48, 5000, 3),     # several splits
+    (2, 64, 4096, 8),     # every row of the staged query block
+    (1, 64, 300, 5),      # more splits than tiles: empty splits
+    (1, 40, 20000, 2),    # long splits: the copy ring wraps many times
 ]
 
 
@@ -58,7 +64,7 @@ def test_mla_decode(case, a):
     check_mla(inp.q, inp.kv, scale=SCALE, lam=min(1.0, a / Lk), num_splits=S)
 
 
-@pytest.mark.parametrize("Hq", [16, 32])
+@pytest.mark.parametrize("Hq", [16, 32, 64])
 def test_mla_random_scores_many_decisions(Hq):
     """Plain N(0,1) inputs: margins spread out around the threshold."""
     from _parity import check_mla
@@ -70,7 +76,7 @@ def test_mla_random_scores_many_decisions(Hq):
         check_mla(q, kv, scale=576 ** -0.5, lam=lam, num_splits=3)
 
 
-@pytest.mark.parametrize("Hq", [16, 32])
+@pytest.mark.parametrize("Hq", [16, 32, 64])
 def test_mla_count_only_matches_the_full_launch(Hq):
     from block_sparse_attention_sm_gb300 import capi
 
@@ -104,7 +110,7 @@ def test_mla_calibration_hits_the_target():
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name", ["mla_decode_32k", "mla_decode_32k_32h"])
+@pytest.mark.parametrize("name", ["mla_decode_32k", "mla_decode_32k_32h", "mla_decode_32k_64h"])
 def test_mla_full_size_sampled(name):
     """The bench's workloads (128 sequences x 32K keys, 4 splits, 16 or 32
     heads) at lambda for 70% skipped tiles; the oracle checks the first, last
@@ -204,6 +210,8 @@ PAGED = [
     (2, 16, [4096, 2500], 1),
     (3, 32, [1000, 0, 3000], 3),        # two softmax warpgroups
     (2, 20, [129, 4096], 2),
+    (3, 64, [1000, 0, 3000], 3),        # heads as MMA rows, two CTAs per split
+    (2, 36, [129, 4096], 2),
 ]
 
 
