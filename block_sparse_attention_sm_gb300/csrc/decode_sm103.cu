@@ -35,6 +35,7 @@
 #include <cuda_bf16.h>
 
 #include "common.cuh"
+#include "decode_rows.cuh"
 #include "ptx_sm103.cuh"
 
 namespace ssattn {
@@ -651,8 +652,18 @@ cudaError_t launch_dec_g(const CUtensorMap& tk, const CUtensorMap& tv, const Dec
 
 cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
                           Mode mode, cudaStream_t st) {
+  if (p.d == 128 && p.G > kDecKeyLayoutMaxG) return launch_decode_rows(tk, tv, p, mode, st);
   return (p.d == 128) ? launch_dec_g<128>(tk, tv, p, mode, st)
                       : launch_dec_g<64>(tk, tv, p, mode, st);
+}
+
+cudaError_t launch_decode_merge(const DecodeParams& p, cudaStream_t st) {
+  const int rows = p.B * p.Hq;
+  if (p.d == 128)
+    decode_merge_kernel<128><<<dim3((rows + 7) / 8), dim3(256), 0, st>>>(p.part, p.o, rows, p.S);
+  else
+    decode_merge_kernel<64><<<dim3((rows + 7) / 8), dim3(256), 0, st>>>(p.part, p.o, rows, p.S);
+  return cudaGetLastError();
 }
 
 }  // namespace ssattn

@@ -9,6 +9,7 @@
 #include <vector>
 
 #include "common.cuh"
+#include "decode_rows.cuh"
 #include "mla.cuh"
 
 namespace ssattn {
@@ -193,7 +194,9 @@ ss_status decode_impl(const void* q, const void* k, const void* v, void* o, int 
   if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Lk < 1 || S < 1 || !scale_ok(scale))
     return SS_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return SS_ERR_UNSUPPORTED;
-  if (Hq / Hkv > 32) return SS_ERR_UNSUPPORTED;  // voting group = MMA N of at most 32 rows
+  // voting group: up to 32 rows (MMA N) with keys on the TMEM lanes, up to
+  // 128 (MMA M) with the heads as rows at d = 128
+  if (Hq / Hkv > (d == 128 ? kDecRowsMaxG : 32)) return SS_ERR_UNSUPPORTED;
   const long nT = ceil_div(Lk, kTile);
   const long ctas = static_cast<long>(B) * Hkv * S;
   if (ctas > 0x7fffffffL) return SS_ERR_INVALID_ARG;
@@ -508,7 +511,7 @@ ss_status ss_attn_decode_paged(const void* q, const void* k_pages, const void* v
       num_kv_splits < 1 || !scale_ok(scale) || !(lambda_a >= 0.f) || !std::isfinite(lambda_a))
     return SS_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return SS_ERR_UNSUPPORTED;
-  if (Hq / Hkv > 32) return SS_ERR_UNSUPPORTED;
+  if (Hq / Hkv > (d == 128 ? kDecRowsMaxG : 32)) return SS_ERR_UNSUPPORTED;
   const int S = num_kv_splits;
   if (static_cast<long>(B) * Hkv * S > 0x7fffffffL ||
       static_cast<long>(num_pages) * Hkv > 0x7fffffffL ||

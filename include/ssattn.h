@@ -60,9 +60,10 @@ extern "C" {
 typedef enum {
   SS_OK = 0,
   SS_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad shape, lambda or scale */
-  SS_ERR_UNSUPPORTED = 2,  /* d not in {64,128}, decode with Hq/Hkv > 32, latent decode
-                              with other widths or Hq > 32, latent prefill with widths
-                              other than 192/128, or the current device is not sm_103 */
+  SS_ERR_UNSUPPORTED = 2,  /* d not in {64,128}, decode with Hq/Hkv > 128 (> 32 at
+                              d = 64), latent decode with other widths or Hq > 64,
+                              latent prefill with widths other than 192/128, or the
+                              current device is not sm_103 */
   SS_ERR_CUDA = 3,         /* a CUDA runtime call failed (launch, copy, sync) */
   SS_ERR_TIMEOUT = 4,      /* a kernel's bounded wait expired (logic error; reported, not hung) */
   SS_ERR_WORKSPACE = 5     /* decode workspace missing or too small */
@@ -166,7 +167,9 @@ size_t ss_attn_decode_workspace_size(int B, int Hq, int d, int num_kv_splits);
  * first tile is always kept), streams all of its K, loads V only for kept
  * tiles, and writes a partial (m, l, O); a second kernel merges the
  * partials by log-sum-exp into bf16 o.  The G = Hq/Hkv query heads of a KV
- * head vote together on each tile; G <= 32 (SS_ERR_UNSUPPORTED above).
+ * head vote together on each tile; G <= 128 at d = 128 (groups above 16
+ * heads run with the heads as the rows of the MMAs), G <= 32 at d = 64
+ * (SS_ERR_UNSUPPORTED above).
  *   skip_counts: nullable device buffer [B*Hkv*num_kv_splits] (skipped tiles
  *     per (sequence, KV head, split)); overwritten.
  *   workspace: device buffer of at least

@@ -91,7 +91,8 @@ def test_prefill_rejects_before_launch(capi, kw, expect):
 @pytest.mark.parametrize("kw,expect", [
     (dict(S=0), "SS_ERR_INVALID_ARG"),
     (dict(Lk=0), "SS_ERR_INVALID_ARG"),
-    (dict(Hq=66, Hkv=2), "SS_ERR_UNSUPPORTED"),       # vote group > 32
+    (dict(Hq=258, Hkv=2), "SS_ERR_UNSUPPORTED"),      # vote group > 128 (MMA rows)
+    (dict(Hq=66, Hkv=2, d=64), "SS_ERR_UNSUPPORTED"),  # vote group > 32 at d = 64
     (dict(S=4, ws=None), "SS_ERR_WORKSPACE"),
     (dict(S=4, ws_bytes=16), "SS_ERR_WORKSPACE"),
 ])
@@ -113,7 +114,8 @@ def test_decode_rejects_before_launch(capi, kw, expect):
     (dict(a=float("inf")), "SS_ERR_INVALID_ARG"),
     (dict(k=FAKE + 4), "SS_ERR_INVALID_ARG"),
     (dict(d=96), "SS_ERR_UNSUPPORTED"),
-    (dict(Hq=66, Hkv=2), "SS_ERR_UNSUPPORTED"),
+    (dict(Hq=258, Hkv=2), "SS_ERR_UNSUPPORTED"),
+    (dict(Hq=66, Hkv=2, d=64), "SS_ERR_UNSUPPORTED"),
     (dict(S=4, ws=None), "SS_ERR_WORKSPACE"),
 ])
 def test_paged_decode_rejects_before_launch(capi, kw, expect):

@@ -34,6 +34,12 @@ SHAPES = [
     (2, 32, 1, 3000, 128, 3),   # G = 32: MQA with 32 query heads (the largest vote group)
     (2, 48, 2, 1300, 64, 2),    # G = 24 (padded to 32 rows), d = 64
     (1, 17, 1, 640, 128, 1),    # G = 17: the smallest group of the 32-row MMA
+    # d = 128 groups above 16 heads: the heads as MMA rows
+    (1, 33, 1, 700, 128, 1),    # G = 33: a warp with one head
+    (2, 96, 2, 900, 128, 4),    # G = 48, two KV heads
+    (2, 64, 1, 3000, 128, 3),   # G = 64 (MQA with 64 query heads)
+    (1, 128, 1, 1500, 128, 2),  # G = 128: every row of the MMA
+    (1, 40, 1, 300, 128, 8),    # more splits than tiles: empty splits
 ]
 
 

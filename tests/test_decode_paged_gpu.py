@@ -122,6 +122,8 @@ CASES = [
     (2, 16, 1, 128, [2500, 4096], 4),          # G = 16
     (4, 32, 8, 128, [333, 8191, 8192, 1], 8),  # Llama-shaped heads, ragged lengths
     (3, 32, 1, 128, [4000, 129, 2048], 2),     # G = 32 (MQA)
+    (3, 64, 1, 128, [4000, 129, 2048], 2),     # G = 64 (MQA, heads as MMA rows)
+    (2, 96, 2, 128, [1000, 2500], 3),          # G = 48
 ]
 
 
