@@ -56,6 +56,7 @@ def _src_hash(names):
 
 
 PAIR_SOURCES = ["prefill_pair_sm103.cu", "ptx_pair_sm103.cuh", "ptx_sm103.cuh", "common.cuh"]
+DECODE_SOURCES = ["decode_sm103.cu", "decode_rows.cuh", "ptx_sm103.cuh", "common.cuh"]
 
 
 def _traffic(kernel, sources):
@@ -516,7 +517,7 @@ def run_native(args):
             "roofline_decode": {
                 "bound": "hbm", "achieved": round(achieved_d, 1), "peak": peaks["hbm"],
                 "unit": "GB/s", "frac": round(achieved_d / peaks["hbm"], 4),
-                "traffic": _traffic("decode", ["decode_sm103.cu", "ptx_sm103.cuh", "common.cuh"]),
+                "traffic": _traffic("decode", DECODE_SOURCES),
                 "kernel": "decode_kernel<128,4,Sparse> + decode_merge_kernel",
                 "peak_kind": f"HBM copy, read+write ({peaks['src']})",
                 "read_stream_gbs": round(read_gbs, 1),
