@@ -40,11 +40,10 @@ struct MlaParams {
   float lambda_a;
 };
 
+// Heads 1..32: keys on the TMEM lanes (one softmax warpgroup of 16 heads up
+// to 16 heads, two above).
 cudaError_t launch_mla_decode(const CUtensorMap& tkv, const MlaParams& p, Mode mode,
                               cudaStream_t st);
-// Heads 17..32: the wide kernel (two softmax warpgroups of 16 heads each).
-cudaError_t launch_mla_decode_wide(const CUtensorMap& tkv, const MlaParams& p, Mode mode,
-                                   cudaStream_t st);
 // Heads 33..64: heads as the MMA rows, O's latent entries split over two CTAs.
 cudaError_t launch_mla_decode_rows(const CUtensorMap& tkv, const MlaParams& p, Mode mode,
                                    cudaStream_t st);

@@ -240,7 +240,6 @@ ss_status decode_impl(const void* q, const void* k, const void* v, void* o, int 
 // The latent-attention decode kernel for the number of heads.
 cudaError_t launch_mla_any(const CUtensorMap& tkv, const MlaParams& p, Mode mode, cudaStream_t st) {
   if (p.Hq > kMlaWideHeads) return launch_mla_decode_rows(tkv, p, mode, st);
-  if (p.Hq > kMlaNarrowHeads) return launch_mla_decode_wide(tkv, p, mode, st);
   return launch_mla_decode(tkv, p, mode, st);
 }
 
