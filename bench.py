@@ -627,10 +627,10 @@ def run_suite(args):
             if s_t > 0 and a > 0:
                 fit_s.append(sk / n_eval)
                 fit_a.append(a)
-            # at d = 128 both prefill kernels run every mode: time each one
-            # explicitly beside the library's own choice
+            # at d = 64 and 128 both prefill kernels run every mode: time each
+            # one explicitly beside the library's own choice
             per_kernel = {}
-            if d == 128:
+            if d in (64, 128):
                 for kname, kid in (("one_cta", 1), ("pair", 2)):
                     def run(kid=kid):
                         st = capi.ss_attn_prefill_ex(q, k, v, o, B, Hq, k.shape[1], Lq, Lk, d,

@@ -7,6 +7,10 @@
 // 128-row query block has exp(scale * (tile_max - m)) < lambda, the tile's
 // exponentials and its P.V are skipped and it adds nothing to l or O.
 //
+// Head widths: d_qk = d_v = 128; d_qk = 192 with d_v = 128 (latent
+// attention); d = 64 with the value tiles padded to 128 columns (the second
+// SM's half of each value tile is a fully out-of-range TMA box, read as zeros).
+//
 // One cluster of two CTAs = query blocks 2p and 2p + 1 of one (b, h_q); the
 // CTAs run on two SMs and share every K/V tile through two-SM MMAs
 // (tcgen05.mma.cta_group::2, M = 256: each SM computes its own block's 128
@@ -105,8 +109,8 @@ struct PairCfg {
   static constexpr int kKHalfBytes = 64 * DQK * 2;      // 64 keys of a tile
   static constexpr int kKChunk = 64 * 128;               // one 64-column chunk of 64 keys
   static constexpr int kVHalfBytes = kTile * 64 * 2;    // 64 value columns of a tile
-  static constexpr int kNK = (DQK == 128) ? 6 : 4;       // K ring slots
-  static constexpr int kNV = (DQK == 128) ? 5 : 4;       // V ring slots
+  static constexpr int kNK = (DQK <= 128) ? 6 : 4;       // K ring slots
+  static constexpr int kNV = (DQK <= 128) ? 5 : 4;       // V ring slots
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + kQBytes;
   static constexpr int kVOff = kKOff + kNK * kKHalfBytes;
@@ -144,12 +148,16 @@ struct PairCtl {
   float2 fin[2][kTile];        // per warpgroup and row: (m_ref, l) at the end
 };
 
-template <int DQK, int DV, Mode MODE>
+// DVO: the value (and output) width in memory.  DVO = 64 runs as DV = 128
+// with the second SM's half of every value tile a fully out-of-range TMA box
+// (read as zeros): O's columns 64.. stay zero and are not written.
+template <int DQK, int DV, int DVO, Mode MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     prefill_pair_kernel(const __grid_constant__ CUtensorMap tmQ,
                         const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
   using C = PairCfg<DQK, DV>;
+  static_assert(DVO == DV || (DVO == 64 && DV == 128), "value width");
   constexpr int NK = C::kNK, NV = C::kNV;
   using Ctl = PairCtl<NK, NV>;
   static_assert(sizeof(Ctl) <= C::kCtlBytes, "control block overflow");
@@ -631,11 +639,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ok = wwait(&ctl->o_full, 0);
       tc_fence_after();
     }
-    if (kPV && ok && has_unit) {
+    if (kPV && ok && has_unit && g * (DV / 2) < DVO) {
       // Epilogue: this warpgroup's half of the row's O / l -> bf16 (a row that
       // saw no key writes zeros).
       const float inv_l = (l_row > 0.f) ? 1.f / l_row : 0.f;
-      __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * p.Lq + grow) * DV + g * (DV / 2);
+      __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * p.Lq + grow) * DVO + g * (DV / 2);
 #pragma unroll 1
       for (int c = 0; c < DV / 64; ++c) {
         uint32_t orr[32];
@@ -687,11 +695,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (tid == 0 && *abort_flag) report_timeout(p.status);
 }
 
-template <int DQK, int DV, Mode MODE>
+template <int DQK, int DV, int DVO, Mode MODE>
 cudaError_t launch_pair(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                         const PrefillParams& p, cudaStream_t st) {
   using C = PairCfg<DQK, DV>;
-  auto* fn = prefill_pair_kernel<DQK, DV, MODE>;
+  auto* fn = prefill_pair_kernel<DQK, DV, DVO, MODE>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
   const long pairs = static_cast<long>(p.B) * p.Hq * ((p.nQB + 1) / 2);
@@ -706,15 +714,22 @@ cudaError_t launch_prefill_pair(int dqk, Mode mode, const CUtensorMap& tq, const
                                 const CUtensorMap& tv, const PrefillParams& p, cudaStream_t st) {
   if (dqk == 192) {
     switch (mode) {
-      case Mode::kDense: return launch_pair<192, 128, Mode::kDense>(tq, tk, tv, p, st);
-      case Mode::kSparse: return launch_pair<192, 128, Mode::kSparse>(tq, tk, tv, p, st);
-      default: return launch_pair<192, 128, Mode::kCount>(tq, tk, tv, p, st);
+      case Mode::kDense: return launch_pair<192, 128, 128, Mode::kDense>(tq, tk, tv, p, st);
+      case Mode::kSparse: return launch_pair<192, 128, 128, Mode::kSparse>(tq, tk, tv, p, st);
+      default: return launch_pair<192, 128, 128, Mode::kCount>(tq, tk, tv, p, st);
+    }
+  }
+  if (dqk == 64) {
+    switch (mode) {
+      case Mode::kDense: return launch_pair<64, 128, 64, Mode::kDense>(tq, tk, tv, p, st);
+      case Mode::kSparse: return launch_pair<64, 128, 64, Mode::kSparse>(tq, tk, tv, p, st);
+      default: return launch_pair<64, 128, 64, Mode::kCount>(tq, tk, tv, p, st);
     }
   }
   switch (mode) {
-    case Mode::kDense: return launch_pair<128, 128, Mode::kDense>(tq, tk, tv, p, st);
-    case Mode::kSparse: return launch_pair<128, 128, Mode::kSparse>(tq, tk, tv, p, st);
-    default: return launch_pair<128, 128, Mode::kCount>(tq, tk, tv, p, st);
+    case Mode::kDense: return launch_pair<128, 128, 128, Mode::kDense>(tq, tk, tv, p, st);
+    case Mode::kSparse: return launch_pair<128, 128, 128, Mode::kSparse>(tq, tk, tv, p, st);
+    default: return launch_pair<128, 128, 128, Mode::kCount>(tq, tk, tv, p, st);
   }
 }
 

@@ -128,19 +128,22 @@ ss_status prefill_impl(const void* q, const void* k, const void* v, void* o, int
   //  - the CTA-pair kernel (two-SM MMAs, one pass) for the dense and voting
   //    paths at d = 128 and for every mode at d_qk = 192 / d_v = 128;
   //  - the one-CTA kernel (two query blocks per CTA; decisions of a run of
-  //    tiles first, kept tiles second) for counting at d = 128 and for
-  //    d = 64.  Measured on GB300 (DiT 32K, Llama 16K causal, chunked 2K on
-  //    32K, 128K): the pair kernel is ahead from dense up to ~70% skipped
-  //    tiles (by 10-20% at 50%), the one-CTA kernel ahead at ~90% (by
-  //    ~25%), where its vote pass runs the score MMAs near the tensor peak;
-  //    the kernel can be chosen explicitly through ss_debug_opts.
+  //    tiles first, kept tiles second) for counting (calibration) at d = 128
+  //    and for every mode at d = 64.  Measured on GB300 (DiT 32K, Llama 16K
+  //    causal, chunked 2K on 32K, 128K): at d = 128 the pair kernel is ahead
+  //    from dense up to ~70% skipped tiles (by 10-20% at 50%), the one-CTA
+  //    kernel ahead at ~90% (by ~25%), where its vote pass runs the score
+  //    MMAs near the tensor peak.  At d = 64 (value tiles padded to 128
+  //    columns in the pair kernel) the two tie dense, the pair kernel leads
+  //    at 50% and the one-CTA kernel at 70% (DiT 32K: 6.46 against 5.97 ms).
+  //    The kernel can be chosen explicitly through ss_debug_opts.
   bool pair = (d == 192) || (d == 128 && mode != Mode::kCount);
   // A shortened vote run (test only) exercises the one-CTA kernel's multi-run path.
-  if (d == 128 && dbg != nullptr && dbg->vote_chunk_tiles != 0) pair = false;
+  if (d != 192 && dbg != nullptr && dbg->vote_chunk_tiles != 0) pair = false;
   const int which = dbg != nullptr ? dbg->prefill_kernel : 0;
   if (which < 0 || which > 2) return SS_ERR_INVALID_ARG;
   if (which != 0) {
-    if ((which == 1 && d == 192) || (which == 2 && d == 64)) return SS_ERR_UNSUPPORTED;
+    if (which == 1 && d == 192) return SS_ERR_UNSUPPORTED;
     pair = (which == 2);
   }
   CUtensorMap tq, tk, tv;

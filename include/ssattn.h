@@ -96,20 +96,20 @@ typedef struct {
      tiles, and carries the softmax state from run to run; a value in
      [1, 2048] shortens the run so that short inputs take the multi-run
      path.  Results do not depend on it (up to rounding).  It applies to the
-     one-CTA kernel, which a nonzero value selects at d = 128 (unless
+     one-CTA kernel, which a nonzero value selects at d = 64 and 128 (unless
      prefill_kernel asks for the pair kernel, which ignores it). */
   int vote_chunk_tiles;
   /* Prefill only (0 otherwise): which of the library's two prefill kernels
      computes the pass.  1 selects the one-CTA kernel (two query blocks per
      CTA; the decisions of a run of tiles first, kept tiles second), 2 the
-     CTA-pair kernel (two-SM MMAs, one pass).  0 chooses automatically: the
-     pair kernel for the dense and voting paths at d = 128 (ahead from dense
-     up to ~70% skipped tiles), the one-CTA kernel for counting at d = 128
-     and for d = 64.  At ~90% skipped tiles and above the one-CTA kernel is
-     the faster one at d = 128.  Decisions and counts do not depend on the
-     kernel; outputs agree up to rounding.  d = 64 has only the one-CTA
-     kernel and d_qk = 192 only the pair kernel: asking for the other
-     returns SS_ERR_UNSUPPORTED. */
+     CTA-pair kernel (two-SM MMAs, one pass).  0 chooses automatically: at
+     d = 128 the pair kernel for the dense and voting paths (ahead from dense
+     up to ~70% skipped tiles) and the one-CTA kernel for counting; at d = 64
+     the one-CTA kernel (ahead at ~70% skipped tiles; the pair kernel leads
+     at ~50%).  At ~90% skipped tiles and above the one-CTA kernel is the
+     faster one.  Decisions and counts do not depend on the kernel; outputs
+     agree up to rounding.  d_qk = 192 has only the pair kernel: asking for
+     the other returns SS_ERR_UNSUPPORTED. */
   int prefill_kernel;
 } ss_debug_opts;
 
