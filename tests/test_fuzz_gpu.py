@@ -79,3 +79,37 @@ def test_mla_random_shapes(seed):
     inp = synth.mla_decode_inputs(B=B, Hq=Hq, Lk=Lk, hot_frac=float(rng.uniform(0.05, 0.4)),
                                   seed=seed, device="cuda")
     check_mla(inp.q, inp.kv, scale=192 ** -0.5, lam=_lam(rng, Lk), num_splits=S)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_decode_random_large_groups(seed):
+    """Vote groups of 17..128 heads at d = 128 (the heads as MMA rows),
+    including groups that leave a warp partly empty."""
+    from _parity import check_decode, hot_decode
+
+    rng = np.random.default_rng(2500 + seed)
+    Hkv = int(rng.choice([1, 2]))
+    G = int(rng.choice([17, 24, 33, 40, 64, 100, 128]))
+    B = int(rng.integers(1, 3))
+    Lk = int(rng.integers(1, 5000))
+    S = int(rng.integers(1, 7))
+    inp = hot_decode(B, Hkv * G, Hkv, Lk, 128, frac=float(rng.uniform(0.05, 0.4)), seed=seed)
+    check_decode(inp.q, inp.k, inp.v, scale=1.0 / math.sqrt(128), lam=_lam(rng, Lk),
+                 num_splits=S)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_mla_random_shapes_many_heads(seed):
+    """Latent-attention decode with 33..64 heads (heads as MMA rows, the
+    latent entries of O over two CTAs)."""
+    from _parity import check_mla
+    from block_sparse_attention_sm_gb300 import synth
+
+    rng = np.random.default_rng(3500 + seed)
+    B = int(rng.integers(1, 3))
+    Hq = int(rng.integers(33, 65))
+    Lk = int(rng.integers(1, 5000))
+    S = int(rng.integers(1, 6))
+    inp = synth.mla_decode_inputs(B=B, Hq=Hq, Lk=Lk, hot_frac=float(rng.uniform(0.05, 0.4)),
+                                  seed=seed, device="cuda")
+    check_mla(inp.q, inp.kv, scale=192 ** -0.5, lam=_lam(rng, Lk), num_splits=S)
