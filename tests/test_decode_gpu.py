@@ -40,6 +40,9 @@ SHAPES = [
     (2, 64, 1, 3000, 128, 3),   # G = 64 (MQA with 64 query heads)
     (1, 128, 1, 1500, 128, 2),  # G = 128: every row of the MMA
     (1, 40, 1, 300, 128, 8),    # more splits than tiles: empty splits
+    (2, 8, 2, 1, 128, 2),       # a single key (the second split is empty)
+    (1, 40, 1, 1, 128, 1),      # a single key, heads as MMA rows
+    (1, 4, 4, 1, 64, 1),        # a single key, d = 64
 ]
 
 

@@ -51,6 +51,8 @@ CASES = [
     (2, 64, 4096, 8),     # every row of the staged query block
     (1, 64, 300, 5),      # more splits than tiles: empty splits
     (1, 40, 20000, 2),    # long splits: the copy ring wraps many times
+    (1, 48, 1, 2),        # a single key (the second split is empty)
+    (2, 24, 1, 1),        # a single key, two softmax warpgroups
 ]
 
 

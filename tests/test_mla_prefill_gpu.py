@@ -39,6 +39,7 @@ SHAPES = [
     (2, 2, 1, 640, 640, False),       # MQA, batch of two
     (1, 2, 2, 129, 129, False),       # one row past a block (odd block count)
     (1, 2, 2, 400, 250, True),        # Lq > Lk: first rows see no key
+    (2, 2, 1, 1, 200, True),          # a single query row (causal: it sees every key)
 ]
 
 

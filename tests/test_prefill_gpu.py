@@ -37,6 +37,8 @@ RAGGED = [
     (1, 2, 2, 400, 250, 64, True),       # Lq > Lk: first rows see no key -> zeros
     (1, 3, 3, 77, 1, 128, False),        # a single key
     (1, 2, 1, 640, 1536, 128, False),    # several full tiles
+    (2, 2, 1, 1, 300, 128, True),        # a single query row (causal: it sees every key)
+    (1, 2, 2, 1, 1, 64, False),          # one query row, one key
 ]
 
 
