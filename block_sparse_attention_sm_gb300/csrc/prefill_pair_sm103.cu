@@ -130,8 +130,8 @@ struct PairCtl {
   uint64_t k_empty[NK];        // each CTA: its K slot may be refilled
   uint64_t v_empty[NV];        // each CTA: its V slot may be refilled
   uint64_t s_full[kNB];        // each CTA: scores of the buffer's tile are in TMEM
-  uint64_t dec_local[kNB];     // leader: the 4 warps on the buffer's tile have decided it
-  uint64_t dec_peer[kNB];      // leader: CTA 1's 4 warps' decisions (16 bytes) have arrived
+  uint64_t dec[kNB];           // leader: both CTAs' 4 warps on the buffer's tile have decided
+                               // it (CTA 0's by arrivals, CTA 1's as 16 bytes of stores)
   uint64_t drain[kSoftWarps];  // each CTA, per softmax warp: the P.V MMAs issued so far are done
   uint64_t rescaled[2][kSoftWarps];  // leader: (CTA, warp) has rescaled its part of O
   uint64_t s_free[kNB];        // leader: the buffer's P.V is issued (or not needed)
@@ -222,8 +222,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < kNB; ++s) {
       mbar_init(&ctl->s_full[s], 1);
-      mbar_init(&ctl->dec_local[s], kGroupWarps);
-      mbar_init(&ctl->dec_peer[s], 1);
+      // this CTA's 4 warps + the score issuer's arrival (which sets the 16
+      // bytes that CTA 1's 4 warps complete)
+      mbar_init(&ctl->dec[s], kGroupWarps + 1);
 
     }
     for (int w = 0; w < kSoftWarps; ++w) {
@@ -309,9 +310,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         mma2_commit_mc(&ctl->s_full[bsel], 3);
         mma2_commit_mc(&ctl->k_empty[s], 3);
-        // CTA 1's four warps on this tile complete 4 bytes each on dec_peer;
-        // this arrival (the phase's one expected arrival) sets that count.
-        mbar_arrive_expect_tx(&ctl->dec_peer[bsel], 4 * kGroupWarps);
+        // CTA 1's four warps on this tile complete 4 bytes each on dec; this
+        // arrival sets that count for the tile's phase.
+        mbar_arrive_expect_tx(&ctl->dec[bsel], 4 * kGroupWarps);
       }
       // Every MMA issued must have finished before TMEM is freed.
       mma2_commit_mc(&ctl->mma_done[0], 1);
@@ -336,8 +337,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        if (!mbar_wait_pair(&ctl->dec_local[bsel], ph, abort_flag, peer_abort) ||
-            !mbar_wait_pair(&ctl->dec_peer[bsel], ph, abort_flag, peer_abort)) {
+        if (!mbar_wait_pair(&ctl->dec[bsel], ph, abort_flag, peer_abort)) {
           ok = false;
           break;
         }
@@ -588,10 +588,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t f = (kept ? kFlagKept : 0u) | (resc ? kFlagRescale : 0u);
         if (leader) {
           *reinterpret_cast<volatile uint32_t*>(&ctl->flags[bsel][q4]) = f;
-          mbar_arrive(&ctl->dec_local[bsel]);
+          mbar_arrive(&ctl->dec[bsel]);
         } else {
           st_async_u32(map_shared(smem_u32(&ctl->peer_flags[bsel][q4]), 0u), f,
-                       lead(&ctl->dec_peer[bsel]));
+                       lead(&ctl->dec[bsel]));
         }
       }
       if (kPV && resc) {
