@@ -361,7 +361,10 @@ def run_native(args):
     h2d = sum(t_.numel() * t_.element_size() for t_ in (hq_, hk_, hv_, h_dq, h_knew, h_vnew))
     d2h = ho_[0].numel() * ho_[0].element_size() + hdo_[0].numel() * hdo_[0].element_size()
     bufs = [(q, k, v, o), tuple(torch.empty_like(t_) for t_ in (q, k, v, o))]
-    dbufs = [tuple(torch.empty_like(t_) for t_ in (dq, h_knew, h_vnew, do)) for _ in range(2)]
+    # (device buffers: empty_like of the pinned host rows would give pageable
+    # host tensors, whose copies block the host and serialise the pipeline)
+    dbufs = [tuple(torch.empty(t_.shape, dtype=t_.dtype, device=dev)
+                   for t_ in (dq, h_knew, h_vnew, do)) for _ in range(2)]
     s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
     ev_in, ev_done, ev_out = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
 
